@@ -1,0 +1,479 @@
+"""Throughput of one attention step over a paged KV pool on GB300.
+
+A step is one pass of the whole hot path over the mixed continuous-batching workload:
+KV append of all 2304 new tokens through the slot mapping, paged decode of 256 requests
+(64 of them sharing a 2048-token prefix on the same pages; long requests split and merged by
+log-sum-exp), and ragged extend of 4 chunked-prefill chunks of 512 tokens over cached prefixes.
+Shapes are Qwen3-8B attention (32 query heads, 8 KV heads, head_dim 128), page size 16, bf16.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the same workload
+instead (a bounded sample per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% HBM peak); extend TFLOP/s (% bf16 peak); attn tokens/s"
+WORKLOAD_IDX = 5
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work of the workload (from the generated lengths)
+# ---------------------------------------------------------------------------------------------
+def workload_counts(b):
+    import numpy as np
+
+    Hkv, D, Hq = b.num_kv_heads, b.head_dim, b.num_q_heads
+    row = Hkv * D * 2  # bytes of one token's K (or V) row
+    ps = b.page_size
+    # decode: each physical KV slot read counted once (shared prefix pages once), K and V
+    indptr = b.dec_kv_indptr.numpy()
+    indices = b.dec_kv_indices.numpy().astype(np.int64)
+    lens = b.dec_kv_lens.numpy().astype(np.int64)
+    slots = []
+    for r in range(len(lens)):
+        pos = np.arange(lens[r])
+        slots.append(indices[indptr[r] + pos // ps] * ps + pos % ps)
+    uniq = np.unique(np.concatenate(slots)).size if slots else 0
+    logical = int(lens.sum())
+    qo_bytes = len(lens) * Hq * D * 2 * 2 + len(lens) * Hq * 4  # q in, out + lse
+    meta = (indptr.size + indices.size + lens.size) * 4
+    dec_bytes = uniq * row * 2 + qo_bytes + meta
+    dec_bytes_logical = logical * row * 2 + qo_bytes + meta
+    # extend: unmasked (query, key) pairs, 2 matmuls of 2*D flops each per pair and head
+    qo = b.ext_qo_indptr.numpy().astype(np.int64)
+    pref = b.ext_prefix_lens.numpy().astype(np.int64)
+    pairs = 0
+    for r in range(len(pref)):
+        E = qo[r + 1] - qo[r]
+        pairs += E * pref[r] + E * (E + 1) // 2
+    ext_flops = 4 * D * Hq * pairs
+    T = b.num_new_tokens
+    app_bytes = T * row * 2 * 2 + T * 8  # read new K/V, write K/V rows, slots
+    tokens = len(lens) + int(qo[-1])
+    return {"decode_bytes": int(dec_bytes), "decode_bytes_logical": int(dec_bytes_logical),
+            "decode_kv_tokens_unique": int(uniq), "decode_kv_tokens_logical": logical,
+            "extend_flops": int(ext_flops), "extend_pairs": int(pairs), "append_bytes": int(app_bytes),
+            "attn_tokens": int(tokens)}
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks sampled by nvidia-smi during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_attention_10_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record():
+    """DRAM bytes per decode launch from the committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != _kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_attention_10_gb300 as pkv
+    from workloads import make_config
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()
+    b = make_config(WORKLOAD_IDX)
+    counts = workload_counts(b)
+    st = torch.cuda.Stream(device=dev)
+
+    # device-resident state: the pool (the KV cache) and this step's inputs
+    kp, vp = b.k_pool.to(dev), b.v_pool.to(dev)
+    dq = b.dec_q.to(dev)
+    d_ind, d_idx, d_len = b.dec_kv_indptr.to(dev), b.dec_kv_indices.to(dev), b.dec_kv_lens.to(dev)
+    eq = b.ext_q.to(dev)
+    e_qo, e_ind, e_idx, e_pre = (b.ext_qo_indptr.to(dev), b.ext_kv_indptr.to(dev),
+                                 b.ext_kv_indices.to(dev), b.ext_prefix_lens.to(dev))
+    kn, vn, sm = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
+    d_out = torch.empty_like(dq)
+    d_lse = torch.empty((b.num_decode, b.num_q_heads), dtype=torch.float32, device=dev)
+    e_out = torch.empty_like(eq)
+    e_lse = torch.empty((eq.shape[0], b.num_q_heads), dtype=torch.float32, device=dev)
+    ws_bytes = pkv.decode_workspace_size(b.num_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, dev)
+    dws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    max_e = b.max_extend_len
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(st)
+        pkv.kv_append(kp, vp, kn, vn, sm, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+        pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
+                         workspace=dws, stream=st)
+        if ev is not None:
+            ev[2].record(st)
+        pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
+                         lse=e_lse, stream=st)
+        if ev is not None:
+            ev[3].record(st)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(st):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region ----------------------------------------------------
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    with torch.cuda.stream(st):
+        start.record(st)
+        for k in range(K):
+            step(evs[k])
+        stop.record(st)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    t_app = [e[0].elapsed_time(e[1]) for e in evs]
+    t_dec = [e[1].elapsed_time(e[2]) for e in evs]
+    t_ext = [e[2].elapsed_time(e[3]) for e in evs]
+
+    # ---- end to end through the public API with host buffers -----------------------------
+    host_in = {n: t.pin_memory() for n, t in (("dq", b.dec_q), ("eq", b.ext_q), ("kn", b.k_new),
+                                               ("vn", b.v_new), ("sm", b.slot_mapping),
+                                               ("d_ind", b.dec_kv_indptr), ("d_idx", b.dec_kv_indices),
+                                               ("d_len", b.dec_kv_lens), ("e_qo", b.ext_qo_indptr),
+                                               ("e_ind", b.ext_kv_indptr), ("e_idx", b.ext_kv_indices),
+                                               ("e_pre", b.ext_prefix_lens))}
+    dev_in = {"dq": dq, "eq": eq, "kn": kn, "vn": vn, "sm": sm, "d_ind": d_ind, "d_idx": d_idx,
+              "d_len": d_len, "e_qo": e_qo, "e_ind": e_ind, "e_idx": e_idx, "e_pre": e_pre}
+    host_out = {"d_out": torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory(),
+                "d_lse": torch.empty(d_lse.shape, dtype=d_lse.dtype).pin_memory(),
+                "e_out": torch.empty(e_out.shape, dtype=e_out.dtype).pin_memory(),
+                "e_lse": torch.empty(e_lse.shape, dtype=e_lse.dtype).pin_memory()}
+    dev_out = {"d_out": d_out, "d_lse": d_lse, "e_out": e_out, "e_lse": e_lse}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        step()
+        for n, t in host_out.items():
+            t.copy_(dev_out[n], non_blocking=True)
+
+    K2 = max(1, min(K, 200))
+    with torch.cuda.stream(st):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        s2.record(st)
+        for _ in range(K2):
+            e2e_step()
+        e2.record(st)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = s2.elapsed_time(e2)
+
+    # ---- max over ranks --------------------------------------------------------------------
+    vals = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = float(vals[0]), float(vals[1])
+
+    peaks = _peaks()
+    ms_step = elapsed_ms / K
+    tokens = counts["attn_tokens"]
+    value = tokens * K * ws / (elapsed_ms / 1e3)
+    dec_ms = statistics.mean(t_dec)
+    ext_ms = statistics.mean(t_ext)
+    app_ms = statistics.mean(t_app)
+    dec_gbs = counts["decode_bytes"] / (dec_ms / 1e3) / 1e9
+    ext_tflops = counts["extend_flops"] / (ext_ms / 1e3) / 1e12
+    app_gbs = counts["append_bytes"] / (app_ms / 1e3) / 1e9
+    traffic = _traffic_record()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, seeded lengths and page permutation)",
+        "config": {
+            "workload": "mixed continuous-batching step: kv_append 2304 tokens + paged decode of 256 "
+                        "requests (KV U[512,4096], 64 share a 2048-token prefix) + ragged extend of 4x512 "
+                        "chunked-prefill tokens (prefixes 0/512/1024/1536); Qwen3-8B attention 32q/8kv "
+                        "heads, head_dim 128, page 16",
+            "decode_requests": b.num_decode, "extend_requests": b.num_extend,
+            "new_tokens": b.num_new_tokens, "page_size": b.page_size, "num_pages": b.num_pages,
+            "l2": "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "roofline": {
+            "kernel": "paged_decode (decode + split merge)",
+            "bound": "hbm",
+            "achieved": round(dec_gbs, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+            "traffic": traffic,
+            "algorithmic_bytes": counts["decode_bytes"],
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "fallback",
+        },
+        "kernels": {
+            "decode": {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
+                       "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
+                       "gbs_logical": round(counts["decode_bytes_logical"] / (dec_ms / 1e3) / 1e9, 1)},
+            "extend": {"ms": round(ext_ms, 4), "tflops": round(ext_tflops, 1),
+                       "frac_bf16": round(ext_tflops / peaks["bf16_tflops_sustained"], 4),
+                       "peak_tflops": peaks["bf16_tflops_sustained"], "flops": counts["extend_flops"]},
+            "kv_append": {"ms": round(app_ms, 4), "gbs": round(app_gbs, 1)},
+        },
+        "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle (reported baseline and reference arm)
+# ---------------------------------------------------------------------------------------------
+def _oracle_sample_runner(b, kp, vp):
+    """A bounded slice of the workload for the oracle: (callable(k), tokens per call)."""
+    import oracle
+
+    B = b.num_decode
+    qo = b.ext_qo_indptr.tolist()
+    rows_per_call = 8
+
+    def run(k):
+        r = k % B
+        oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
+                            b.page_size, b.sm_scale, requests=[r])
+        e = k % b.num_extend
+        E = qo[e + 1] - qo[e]
+        i0 = (k * rows_per_call) % E
+        # rows_per_call extend queries of chunk e (a contiguous run inside the chunk)
+        sub_qo = [0, min(rows_per_call, E - i0)]
+        import torch as _t
+        q_rows = b.ext_q[qo[e] + i0: qo[e] + i0 + sub_qo[1]]
+        oracle.paged_extend(q_rows, kp, vp, _t.tensor(sub_qo, dtype=_t.int32),
+                            b.ext_kv_indptr[e:e + 2] - b.ext_kv_indptr[e], b.ext_kv_indices[
+                                int(b.ext_kv_indptr[e]):int(b.ext_kv_indptr[e + 1])],
+                            (b.ext_prefix_lens[e:e + 1] + i0).to(_t.int32), b.page_size, b.sm_scale)
+        return 1 + sub_qo[1]
+
+    return run
+
+
+def cpu_baseline(b, seconds=12.0):
+    import oracle
+
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
+    run = _oracle_sample_runner(b, kp, vp)
+    t0 = time.perf_counter()
+    toks, k = 0, 0
+    while time.perf_counter() - t0 < seconds:
+        toks += run(k)
+        k += 1
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(toks / el, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{k} slices of the mixed step, each 1 decode request (all 32 heads) + up to 8 "
+                      f"extend query rows of one chunk; {toks} attention tokens in {el:.1f} s; fp64 NumPy, "
+                      f"BLAS may use all {cores} affinity cores"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    from workloads import make_config
+    import oracle
+
+    b = make_config(WORKLOAD_IDX)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
+    run = _oracle_sample_runner(b, kp, vp)
+    for k in range(args.warmup):
+        run(k)
+    budget = 150.0
+    t0 = time.perf_counter()
+    toks, done = 0, 0
+    for k in range(args.steps):
+        toks += run(k)
+        done += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    val = toks / el
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "steps_completed": done, "warmup": args.warmup,
+            "ms_per_step": round(el / done * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mixed continuous-batching step (bounded oracle sample per step)"},
+            "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: 1 decode request + up to 8 extend query rows of the mixed step"},
+            "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            from workloads import make_config
+
+            line["cpu_baseline"] = cpu_baseline(make_config(WORKLOAD_IDX), args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * pagedkv.h -- C ABI of a GB300 (sm_103a) library for attention over a paged KV pool.
+ *
+ * The operations are the attention layer of an SGLang-style serving engine:
+ *   - the paged pool with its page table and token slots (mini-sglang from Scratch handbook,
+ *     "What you will be able to do": paged KV pool, page table, token pool);
+ *   - K/V of the step's new tokens written into the pool through a slot mapping
+ *     (same handbook, "How this book works": the KV-cache writes);
+ *   - attention that reads each request's KV in place through page indices, page size 1 or
+ *     larger (nanoSGLang README, "Ablation": FlashInfer paged attention, zero-copy KV;
+ *     mini-sglang README, "KVcache Management": page size == 1 and > 1);
+ *   - GQA and causal attention offset by the cached prefix (Mini-SGLang README,
+ *     "Reference Attention Backends", torch backend), with radix-cache prefix pages shared
+ *     between requests (mini-sglang README, "KVcache Management": Radix Attention);
+ *   - split-KV partial states and their log-sum-exp merge for long decodes.
+ *
+ * Data layout (all device memory, caller-owned):
+ *   pool K and V  bf16 [num_pages, page_size, num_kv_heads, head_dim], contiguous (NHD pages,
+ *                 nanoSGLang README, "Architecture").  Flat slot s = page * page_size + row.
+ *   page lists    CSR: request b owns pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]), in
+ *                 position order; KV position j of request b is row j % page_size of page
+ *                 kv_indices[kv_indptr[b] + j / page_size].  Pages may appear in several
+ *                 requests' lists (shared prefixes).
+ *   GQA           query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   LSE           natural log of sum_j exp(sm_scale * q . k_j), fp32.
+ *
+ * Calls are asynchronous on the given stream (a cudaStream_t passed as void*, NULL = legacy
+ * default stream), never synchronise the host and never allocate: every scratch buffer
+ * ("workspace") is passed in by the caller, so a call can be captured in a CUDA graph.
+ *
+ * Errors: arguments that can be checked on the host (null pointers, shapes, alignment,
+ * workspace size) return a status and launch nothing.  Kernels bounds-check every page index
+ * and slot they dereference and skip an access that would fall outside the pool; when
+ * err_word is non-NULL they atomically OR a PKV_DEVERR_* bit into that device word.  Waits
+ * inside kernels are bounded and report PKV_DEVERR_TIMEOUT instead of hanging.  The caller
+ * reads err_word when it chooses to (it is never read by the library).
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, negative count, bad shape or misaligned buffer */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, group size or page size */
+  PKV_ERR_WORKSPACE = 3,   /* workspace smaller than the matching *_workspace_size() */
+  PKV_ERR_CUDA = 4         /* a CUDA runtime call failed (launch error, no device) */
+} pkv_status;
+
+/* Bits OR-ed into *err_word by kernels. */
+#define PKV_DEVERR_PAGE_OOB 0x1u /* a page index outside [0, num_pages) was skipped */
+#define PKV_DEVERR_SLOT_OOB 0x2u /* an append slot >= num_pages * page_size was skipped */
+#define PKV_DEVERR_LENGTH 0x4u   /* a KV length exceeds the request's pages, or a decode length is 0 */
+#define PKV_DEVERR_TIMEOUT 0x8u  /* a bounded in-kernel wait gave up */
+#define PKV_DEVERR_INTERNAL 0x10u /* a launch-time invariant failed and the CTA skipped its work */
+
+typedef struct {
+  void* k;              /* bf16 [num_pages, page_size, num_kv_heads, head_dim], 16-byte aligned */
+  void* v;              /* same shape as k */
+  int64_t num_pages;
+  int32_t page_size;    /* >= 1 */
+  int32_t num_kv_heads; /* >= 1 */
+  int32_t head_dim;     /* attention calls: 64 or 128; append/gather: any multiple of 8 */
+} pkv_pool;
+
+/* Human-readable name of a status. */
+const char* pkv_status_string(pkv_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t pkv_version(void);
+
+/*
+ * KV-cache write.  For t < num_tokens: pool.k row slot_mapping[t] = k_new[t] and the same for
+ * V; a negative slot marks a padding token and writes nothing.  A bit-exact copy.
+ *   k_new, v_new  bf16 [num_tokens, num_kv_heads, head_dim] (device)
+ *   slot_mapping  int64 [num_tokens] (device); slots must be distinct within one call
+ *   err_word      nullable device uint32; PKV_DEVERR_SLOT_OOB for slot >= num_pages*page_size
+ */
+pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int32_t num_tokens, uint32_t* err_word,
+                         void* stream);
+
+/*
+ * Page gather (test and debug op): copy every request's K and V rows, in position order, into
+ * contiguous buffers.  Request b occupies rows [sum_{b'<b} kv_lens[b'], ... + kv_lens[b]).
+ *   kv_indptr  int32 [batch_size+1], kv_indices int32 [kv_indptr[batch_size]], kv_lens int32
+ *              [batch_size] (device)
+ *   k_out, v_out  bf16 [sum(kv_lens), num_kv_heads, head_dim] (device)
+ *   err_word   nullable; PKV_DEVERR_PAGE_OOB / PKV_DEVERR_LENGTH, the row is left unwritten
+ */
+pkv_status pkv_paged_gather(const pkv_pool* pool, const int32_t* kv_indptr,
+                            const int32_t* kv_indices, const int32_t* kv_lens, int32_t batch_size,
+                            void* k_out, void* v_out, uint32_t* err_word, void* stream);
+
+/*
+ * Bytes of workspace pkv_paged_decode needs for this shape on the current device (the split
+ * partials, sized by the device's SM count).  Returns 0 for an invalid shape.
+ */
+size_t pkv_decode_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim);
+
+/*
+ * Paged decode: one query per request at its last position, attending over all kv_lens[b]
+ * positions (the KV of the step's own token is appended first with pkv_kv_append).
+ *   q          bf16 [batch_size, num_q_heads, head_dim] (device)
+ *   kv_indptr, kv_indices, kv_lens  as for pkv_paged_gather; kv_lens[b] >= 1
+ *   sm_scale   softmax scale applied to q . k (e.g. 1/sqrt(head_dim))
+ *   out        bf16 [batch_size, num_q_heads, head_dim] (device), round-to-nearest-even
+ *   lse        nullable fp32 [batch_size, num_q_heads] (device)
+ *   workspace  device buffer of at least pkv_decode_workspace_size(...) bytes, 256-byte
+ *              aligned; its contents need no initialisation and are clobbered
+ * Long requests are split across CTAs (flash-decoding) and merged by log-sum-exp in a second
+ * kernel on the same stream.  head_dim 64 or 128, num_q_heads / num_kv_heads <= 16.
+ * A request with kv_lens[b] == 0 gets out = 0, lse = -inf and PKV_DEVERR_LENGTH.
+ */
+pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_size,
+                            int32_t num_q_heads, const int32_t* kv_indptr,
+                            const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            uint32_t* err_word, void* stream);
+
+/*
+ * Bytes of workspace pkv_paged_extend needs (0 when none is needed).
+ */
+size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_extend_len);
+
+/*
+ * Ragged extend (prefill / chunked prefill over a cached prefix).  Request b's queries are rows
+ * qo_indptr[b] .. qo_indptr[b+1] of q; query i of the request is at absolute position
+ * prefix_lens[b] + i and attends to KV positions j <= prefix_lens[b] + i.  The request's KV
+ * length is prefix_lens[b] + (qo_indptr[b+1] - qo_indptr[b]) and all of it is read through the
+ * pool: append the new tokens' K/V first.
+ *   q          bf16 [num_q_tokens, num_q_heads, head_dim] (device)
+ *   num_q_tokens  rows of q and out (= qo_indptr[batch_size])
+ *   qo_indptr  int32 [batch_size+1]; prefix_lens int32 [batch_size] (device)
+ *   max_extend_len  an upper bound of qo_indptr[b+1]-qo_indptr[b] over b (sizes the grid;
+ *              rows beyond it are not computed)
+ *   out        bf16 [num_q_tokens, num_q_heads, head_dim]; lse nullable fp32 [num_q_tokens, num_q_heads]
+ *   workspace  at least pkv_extend_workspace_size(...) bytes (may be NULL when that is 0)
+ * head_dim 128, page_size a power of two >= 8; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ */
+pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
+                            const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
+                            const int32_t* kv_indptr, const int32_t* kv_indices,
+                            const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            uint32_t* err_word, void* stream);
+
+/*
+ * Log-sum-exp merge of split partial states (flash-decoding).  For each row n and head h:
+ *   lse[n,h] = ln sum_s exp(lse_parts[s,n,h]);  out[n,h,:] = sum_s exp(lse_parts[s,n,h] - lse[n,h]) * o_parts[s,n,h,:]
+ * A split with lse_parts = -inf is empty and contributes nothing; if all are empty the row gets
+ * out = 0, lse = -inf.
+ *   o_parts    fp32 [num_splits, num_rows, num_heads, head_dim] (device), each split normalised
+ *              by its own softmax sum
+ *   lse_parts  fp32 [num_splits, num_rows, num_heads] (device)
+ *   out        bf16 [num_rows, num_heads, head_dim]; lse nullable fp32 [num_rows, num_heads]
+ * head_dim a multiple of 4, at most 512.
+ */
+pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
+                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                            float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,264 @@
+"""Python binding of libpagedkv (attention over a paged KV pool on GB300).
+
+Argument marshalling only: every function here checks that the tensors it is given have the
+dtype, device and contiguity the C ABI expects, passes their device pointers and the current
+CUDA stream to the matching ``pkv_*`` entry point, and turns a non-OK status into an exception.
+All computation happens in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+a missing library is an error.
+
+Names follow the C ABI in ``include/pagedkv.h`` (``pkv_kv_append`` -> ``kv_append`` ...).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
+    "paged_decode", "extend_workspace_size", "paged_extend", "merge_states", "status_string",
+    "version", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT",
+    "DEVERR_INTERNAL",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+_lib = None
+
+DEVERR_PAGE_OOB = 0x1
+DEVERR_SLOT_OOB = 0x2
+DEVERR_LENGTH = 0x4
+DEVERR_TIMEOUT = 0x8
+DEVERR_INTERNAL = 0x10
+
+_c_i32, _c_i64, _c_f32, _c_sz, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+
+class Pool(ctypes.Structure):
+    _fields_ = [("k", _vp), ("v", _vp), ("num_pages", _c_i64), ("page_size", _c_i32),
+                ("num_kv_heads", _c_i32), ("head_dim", _c_i32)]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpagedkv.so (built by ``paged_kv_attention_10_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is not built; run paged_kv_attention_10_gb300.build.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.POINTER(Pool)
+    sig = {
+        "pkv_status_string": (ctypes.c_char_p, [_c_i32]),
+        "pkv_version": (_c_i32, []),
+        "pkv_kv_append": (_c_i32, [P, _vp, _vp, _vp, _c_i32, _vp, _vp]),
+        "pkv_paged_gather": (_c_i32, [P, _vp, _vp, _vp, _c_i32, _vp, _vp, _vp, _vp]),
+        "pkv_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32]),
+        "pkv_paged_decode": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp, _vp,
+                                      _c_sz, _vp, _vp]),
+        "pkv_extend_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
+        "pkv_paged_extend": (_c_i32, [P, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_i32,
+                                      _c_f32, _vp, _vp, _vp, _c_sz, _vp, _vp]),
+        "pkv_merge_states": (_c_i32, [_vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().pkv_version())
+
+
+# ---------------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------------
+def _need(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> Pool:
+    _need(k_pool, "k_pool", torch.bfloat16)
+    _need(v_pool, "v_pool", torch.bfloat16, k_pool.device)
+    if k_pool.dim() != 4 or k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool must both be [num_pages, page_size, num_kv_heads, head_dim]")
+    n, ps, hkv, d = k_pool.shape
+    return Pool(k_pool.data_ptr(), v_pool.data_ptr(), n, ps, hkv, d)
+
+
+def _call(fn: str, *args):
+    st = getattr(load(), fn)(*args)
+    if st != 0:
+        raise PagedKVError(fn, st)
+
+
+# ---------------------------------------------------------------------------------------------
+# operations
+# ---------------------------------------------------------------------------------------------
+def kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stream=None) -> None:
+    """Write k_new[t], v_new[t] into pool slot slot_mapping[t] (negative = skip). In place."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(k_new, "k_new", torch.bfloat16, dev)
+    _need(v_new, "v_new", torch.bfloat16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    T = slot_mapping.numel()
+    if k_new.shape != (T, pool.num_kv_heads, pool.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens, num_kv_heads, head_dim]")
+    with torch.cuda.device(dev):
+        _call("pkv_kv_append", ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T,
+              _ptr(err_word), _stream_ptr(stream, dev))
+
+
+def paged_gather(k_pool, v_pool, kv_indptr, kv_indices, kv_lens, total_len: int, err_word=None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Every request's K/V rows in position order, concatenated: [total_len, Hkv, D] each."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    for t, n in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (kv_lens, "kv_lens")):
+        _need(t, n, torch.int32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    B = kv_lens.numel()
+    k_out = torch.empty((total_len, pool.num_kv_heads, pool.head_dim), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty_like(k_out)
+    with torch.cuda.device(dev):
+        _call("pkv_paged_gather", ctypes.byref(pool), _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_lens),
+              B, _ptr(k_out), _ptr(v_out), _ptr(err_word), _stream_ptr(stream, dev))
+    return k_out, v_out
+
+
+def decode_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim, device=None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(load().pkv_decode_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim))
+
+
+def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: float, out=None,
+                 lse=None, workspace=None, err_word=None, stream=None, return_lse=True):
+    """Decode attention of q [B, Hq, D] over each request's paged KV. Returns (out, lse)."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(q, "q", torch.bfloat16, dev)
+    for t, n in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (kv_lens, "kv_lens")):
+        _need(t, n, torch.int32, dev)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        need = int(load().pkv_decode_workspace_size(B, Hq, pool.num_kv_heads, D))
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+        _call("pkv_paged_decode", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
+              _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
+              _ptr(workspace), workspace.numel(), _ptr(err_word), _stream_ptr(stream, dev))
+    return out, lse
+
+
+def extend_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim, max_extend_len,
+                          device=None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(load().pkv_extend_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim,
+                                                    max_extend_len))
+
+
+def paged_extend(q, k_pool, v_pool, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                 max_extend_len: int, sm_scale: float, out=None, lse=None, workspace=None,
+                 err_word=None, stream=None, return_lse=True):
+    """Ragged extend attention with a cached-prefix causal offset. Returns (out, lse)."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(q, "q", torch.bfloat16, dev)
+    for t, n in ((qo_indptr, "qo_indptr"), (kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"),
+                 (prefix_lens, "prefix_lens")):
+        _need(t, n, torch.int32, dev)
+    N, Hq, D = q.shape
+    B = prefix_lens.numel()
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        need = int(load().pkv_extend_workspace_size(B, Hq, pool.num_kv_heads, D, max_extend_len))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", torch.uint8, dev)
+        _call("pkv_paged_extend", ctypes.byref(pool), _ptr(q), N, _ptr(qo_indptr), B, Hq, _ptr(kv_indptr),
+              _ptr(kv_indices), _ptr(prefix_lens), int(max_extend_len), float(sm_scale), _ptr(out),
+              _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+              _ptr(err_word), _stream_ptr(stream, dev))
+    return out, lse
+
+
+def merge_states(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """LSE merge of split partials o_parts [S, N, H, D] fp32, lse_parts [S, N, H] fp32."""
+    dev = o_parts.device
+    _need(o_parts, "o_parts", torch.float32)
+    _need(lse_parts, "lse_parts", torch.float32, dev)
+    S, N, H, D = o_parts.shape
+    if lse_parts.shape != (S, N, H):
+        raise ValueError("lse_parts must be [S, N, H]")
+    if out is None:
+        out = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((N, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _call("pkv_merge_states", _ptr(o_parts), _ptr(lse_parts), S, N, H, D, _ptr(out), _ptr(lse),
+              _stream_ptr(stream, dev))
+    return out, lse

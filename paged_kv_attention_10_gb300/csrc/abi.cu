@@ -1,0 +1,60 @@
+// C-ABI plumbing: status strings, version, host-side argument checks and device properties.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace pkv_host {
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int d = current_device();
+  if (d < 0) return 0;
+  if (d < 64) {
+    int c = cache[d].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+  if (d < 64) cache[d].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+bool valid_pool(const pkv_pool* p) {
+  if (!p || !p->k || !p->v) return false;
+  if (p->num_pages <= 0 || p->page_size <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0) return false;
+  if ((p->head_dim % 8) != 0) return false;
+  if (!aligned16(p->k) || !aligned16(p->v)) return false;
+  return true;
+}
+
+}  // namespace pkv_host
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_WORKSPACE: return "workspace too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int32_t pkv_version(void) { return 100; }  // 0.1.0
+
+}  // extern "C"

@@ -1,0 +1,733 @@
+// Paged decode attention (one query per request) and the split-KV log-sum-exp merge.
+//
+// What it computes: for request b and query head h, attention of q[b,h] over the request's
+// kv_lens[b] KV positions, gathered in place from the paged pool through the CSR page list
+// (nanoSGLang README, "Ablation": paged attention with zero-copy KV; Mini-SGLang README,
+// "Reference Attention Backends": paged KV gather, GQA via repeat_interleave, online softmax in
+// the Triton decode kernel).  Long requests are split and merged by log-sum-exp (flash-decoding).
+//
+// Design for GB300 (HBM-bound: ~2-8 flop per KV byte):
+//  * Persistent grid, one CTA per SM.  The KV of all (request, KV-head-group) units forms one
+//    token stream; every CTA takes an equal contiguous share of it, so work is balanced whatever
+//    the length mix, and a unit cut by a share boundary leaves one partial per CTA that touched
+//    it (merged by a second kernel).  A CTA covers HC KV heads so that one token row of the CTA
+//    is a single contiguous HC*D*2-byte run of the NHD page.
+//  * One producer warp walks the CTA's share and streams token rows with cp.async.bulk into a
+//    ring of NS shared-memory stages (K and V), completion counted in bytes on an mbarrier.
+//    Rows land at a padded stride so the warps' ldmatrix reads are bank-conflict free.
+//  * Consumer warps (one per KV head, W per head when HC < 8) take 16-token slices.  Scores are
+//    computed transposed, S^T = K Q^T, with m16n8k16 bf16 MMAs (tokens fill M=16, the G query
+//    heads of the group fill N=8, so nothing is padded to 16 heads); the online softmax keeps a
+//    running max and sum in fp32 per head; P^T is turned into the B operand of O^T += V^T P^T
+//    by movmatrix.  KV is read exactly once per CTA per token, for all heads of the group.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kSegFirst = 1;    // first stage of this CTA's segment of the unit
+constexpr int kSegLast = 2;     // last stage of the segment
+constexpr int kStartsUnit = 4;  // the segment starts at position 0 of the unit
+constexpr int kEndsUnit = 8;    // the segment ends at the unit's last position
+
+struct StageHdr {
+  int32_t unit;  // -1: no more work
+  int32_t b;
+  int32_t hg;
+  int32_t tok0;
+  int32_t ntok;
+  int32_t flags;
+  int32_t part;
+  int32_t pad;
+};
+
+struct DecodeArgs {
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  const __nv_bfloat16* q;
+  int32_t batch;
+  int32_t num_q_heads;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* kv_lens;
+  float scale_log2;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* unit_first;
+  int32_t* unit_last;
+  uint32_t* err_word;
+  int32_t HC;       // KV heads per CTA
+  int32_t nhg;      // head groups = num_kv_heads / HC
+  int32_t W;        // consumer warps per KV head
+  int32_t group;    // query heads per KV head
+  int32_t row_stride;    // shared-memory bytes per token row
+  int32_t stage_tokens;  // tokens per stage = 16 * W
+  int32_t num_stages;
+  int32_t num_parts;     // partial slots in the workspace
+};
+
+constexpr int kMaxStages = 8;
+
+template <int D, int NT>
+struct Consumer {
+  static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of O^T
+  // floats per lane exchanged when W > 1 warps share a head: m, l and O^T fragments
+  static constexpr int kMergeFloats = 4 * NT + KS * NT * 4;
+};
+
+// ---------------------------------------------------------------------------------------------
+// Producer: walk the CTA's share of the token stream and fill stages.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* hdr,
+                                uint64_t* full, uint64_t* empty) {
+  const int lane = threadIdx.x & 31;
+  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  const int nhg = a.nhg;
+  const uint32_t RB = (uint32_t)a.HC * D * 2;
+  const int64_t row_elems = (int64_t)a.num_kv_heads * D;
+
+  int64_t sumL = 0;
+  for (int i = lane; i < a.batch; i += 32) sumL += max(0, __ldg(a.kv_lens + i));
+  sumL = warp_sum(sumL);
+  const int64_t T = sumL * nhg;
+  int64_t share = (T + gridDim.x - 1) / gridDim.x;
+  share = ((share + 15) / 16) * 16;
+  if (share < 16) share = 16;
+  const int64_t c0 = (int64_t)blockIdx.x * share;
+  const int64_t c1 = min(T, c0 + share);
+
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+
+  auto next_stage = [&]() {
+    if (++stage == NS) {
+      stage = 0;
+      phase ^= 1;
+    }
+  };
+
+  auto emit = [&](int unit, int b, int hg, int tok0, int ntok, int flags) -> bool {
+    if (!mbar_wait(&empty[stage], phase ^ 1)) {
+      if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      return false;
+    }
+    if (lane == 0) {
+      StageHdr h;
+      h.unit = unit;
+      h.b = b;
+      h.hg = hg;
+      h.tok0 = tok0;
+      h.ntok = ntok;
+      h.flags = flags;
+      h.part = blockIdx.x + unit;
+      h.pad = 0;
+      hdr[stage] = h;
+    }
+    uint8_t* kst = stages + (size_t)stage * 2 * Ts * RS;
+    uint8_t* vst = kst + (size_t)Ts * RS;
+    if (unit < 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[stage]);
+      next_stage();
+      return true;
+    }
+    const int32_t p0 = __ldg(a.kv_indptr + b), p1 = __ldg(a.kv_indptr + b + 1);
+    // up to 4 rows per lane (stage_tokens <= 128)
+    int64_t src[4];
+    int nvalid = 0;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = lane + 32 * r;
+      src[r] = -1;
+      if (j < ntok) {
+        const int pos = tok0 + j;
+        const int64_t pslot = (int64_t)p0 + pos / a.page_size;
+        if (pslot >= p1) {
+          bad |= PKV_DEVERR_LENGTH;
+        } else {
+          const int64_t page = __ldg(a.kv_indices + pslot);
+          if (page < 0 || page >= a.num_pages) {
+            bad |= PKV_DEVERR_PAGE_OOB;
+          } else {
+            src[r] = (page * a.page_size + pos % a.page_size) * row_elems + (int64_t)hg * a.HC * D;
+            ++nvalid;
+          }
+        }
+      }
+    }
+    if (bad) report(a.err_word, bad);
+    const int tot = warp_sum(nvalid);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)tot * RB * 2);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if (src[r] >= 0) {
+        const int j = lane + 32 * r;
+        bulk_g2s(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage]);
+        bulk_g2s(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage]);
+      }
+    }
+    next_stage();
+    return true;
+  };
+
+  if (c0 < c1) {
+    int64_t base = 0;  // stream offset of request b0
+    for (int b0 = 0; b0 < a.batch && base < c1 && ok; b0 += 32) {
+      const int b = b0 + lane;
+      const int64_t L = (b < a.batch) ? (int64_t)max(0, __ldg(a.kv_lens + b)) : 0;
+      int64_t incl = L;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int64_t rs = base + nhg * (incl - L);
+      const int64_t re = base + nhg * incl;
+      uint32_t mask = __ballot_sync(0xffffffffu, b < a.batch && L > 0 && re > c0 && rs < c1);
+      while (mask && ok) {
+        const int src_lane = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int bb = b0 + src_lane;
+        const int64_t Lb = __shfl_sync(0xffffffffu, L, src_lane);
+        const int64_t rsb = __shfl_sync(0xffffffffu, rs, src_lane);
+        for (int hg = 0; hg < nhg && ok; ++hg) {
+          const int64_t us = rsb + (int64_t)hg * Lb, ue = us + Lb;
+          const int64_t s0 = max(us, c0), s1 = min(ue, c1);
+          if (s0 >= s1) continue;
+          const int t0 = (int)(s0 - us), t1 = (int)(s1 - us);
+          const int unit = bb * nhg + hg;
+          for (int t = t0; t < t1 && ok; t += Ts) {
+            int flags = 0;
+            if (t == t0) flags |= kSegFirst;
+            if (t + Ts >= t1) flags |= kSegLast;
+            if (t0 == 0) flags |= kStartsUnit;
+            if (t1 == (int)Lb) flags |= kEndsUnit;
+            ok = emit(unit, bb, hg, t, min(Ts, t1 - t), flags);
+          }
+        }
+      }
+      base += nhg * __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (ok) emit(-1, 0, 0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Consumers: 16-token slices of one KV head with its G query heads.
+// ---------------------------------------------------------------------------------------------
+template <int D, int NT>
+__device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* hdr,
+                                uint64_t* full, uint64_t* empty, float* mbuf) {
+  constexpr int KS = D / 16;
+  constexpr int MF = Consumer<D, NT>::kMergeFloats;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HC = a.HC, W = a.W, G = a.group;
+  const int NC = HC * W;
+  const int hl = warp % HC;  // KV head within the CTA's group
+  const int si = warp / HC;  // slice within a stage
+  const int g = lane >> 2, c = lane & 3;
+  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  const int HQU = HC * G;  // query heads per unit
+
+  // per-lane ldmatrix row offsets
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t k_lane_off = (uint32_t)((si * 16 + ri + ((mi & 1) << 3)) * RS + hl * D * 2 + ((mi >> 1) << 3) * 2);
+  const uint32_t v_lane_off = (uint32_t)((si * 16 + ri + ((mi >> 1) << 3)) * RS + hl * D * 2 + ((mi & 1) << 3) * 2);
+  const uint32_t stages_u32 = smem_u32(stages);
+
+  uint32_t qf[NT][KS][2];
+  float o[KS][NT][4];
+  float m[NT][2], l[NT][2];
+
+  int stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    if (!mbar_wait(&full[stage], phase)) {
+      if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      break;
+    }
+    const StageHdr h = hdr[stage];
+    if (h.unit < 0) break;
+
+    if (h.flags & kSegFirst) {
+      // query fragments (B operand of S^T = K Q^T): lane (g, c) holds q[head g][16ks + 2c, +1]
+      // and [16ks + 2c + 8, +9]
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + g;
+        const bool valid = head < G;
+        const __nv_bfloat16* qp =
+            a.q + ((int64_t)h.b * a.num_q_heads + (int64_t)(h.hg * HC + hl) * G + head) * D + 2 * c;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qf[nt][ks][0] = valid ? ld_nc_u32(qp + ks * 16) : 0u;
+          qf[nt][ks][1] = valid ? ld_nc_u32(qp + ks * 16 + 8) : 0u;
+        }
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[mt][nt][i] = 0.f;
+      }
+    }
+
+    const int nv = min(16, h.ntok - si * 16);
+    if (nv > 0) {
+      const uint32_t kb = stages_u32 + (uint32_t)stage * 2 * Ts * RS;
+      const uint32_t vb = kb + (uint32_t)Ts * RS;
+      float s[NT][4], s2[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kb + k_lane_off + ks * 32, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (ks & 1)
+            mma_bf16_16816(s2[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+          else
+            mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+        }
+      }
+      uint32_t bp[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = g + ((i >> 1) << 3);
+          x[i] = (tok < nv) ? (s[nt][i] + s2[nt][i]) * a.scale_log2 : -INFINITY;
+        }
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+        const float corr0 = ex2(m[nt][0] - mn0), corr1 = ex2(m[nt][1] - mn1);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+        const float p0 = ex2(x[0] - mn0), p1 = ex2(x[1] - mn1);
+        const float p2 = ex2(x[2] - mn0), p3 = ex2(x[3] - mn1);
+        l[nt][0] = l[nt][0] * corr0 + p0 + p2;
+        l[nt][1] = l[nt][1] * corr1 + p1 + p3;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][0] *= corr0;
+          o[mt][nt][1] *= corr1;
+          o[mt][nt][2] *= corr0;
+          o[mt][nt][3] *= corr1;
+        }
+        bp[nt][0] = movmatrix_t(pack_bf16x2(p0, p1));
+        bp[nt][1] = movmatrix_t(pack_bf16x2(p2, p3));
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vb + v_lane_off + mt * 32, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+
+    if (h.flags & kSegLast) {
+      if (W > 1) {
+        // combine the W warps that split this head's tokens (all consumer warps reach the
+        // segment end on the same stage)
+        float* buf = mbuf + ((size_t)((si > 0 ? si - 1 : 0) * HC + hl) * MF) * 32 + lane;
+        if (si > 0) {
+          int e = 0;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            buf[(e++) * 32] = m[nt][0];
+            buf[(e++) * 32] = m[nt][1];
+            buf[(e++) * 32] = l[nt][0];
+            buf[(e++) * 32] = l[nt][1];
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) buf[(e++) * 32] = o[mt][nt][i];
+          }
+        }
+        named_bar_sync(1, NC * 32);
+        if (si == 0) {
+          for (int w = 1; w < W; ++w) {
+            const float* ob = mbuf + ((size_t)((w - 1) * HC + hl) * MF) * 32 + lane;
+            int e = 0;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float mw0 = ob[(e++) * 32], mw1 = ob[(e++) * 32];
+              const float lw0 = ob[(e++) * 32], lw1 = ob[(e++) * 32];
+              const float mt0 = fmaxf(m[nt][0], mw0), mt1 = fmaxf(m[nt][1], mw1);
+              const float fa0 = ex2(m[nt][0] - mt0), fa1 = ex2(m[nt][1] - mt1);
+              const float fb0 = ex2(mw0 - mt0), fb1 = ex2(mw1 - mt1);
+              m[nt][0] = mt0;
+              m[nt][1] = mt1;
+              l[nt][0] = l[nt][0] * fa0 + lw0 * fb0;
+              l[nt][1] = l[nt][1] * fa1 + lw1 * fb1;
+#pragma unroll
+              for (int mt = 0; mt < KS; ++mt) {
+                o[mt][nt][0] = o[mt][nt][0] * fa0 + ob[(e++) * 32] * fb0;
+                o[mt][nt][1] = o[mt][nt][1] * fa1 + ob[(e++) * 32] * fb1;
+                o[mt][nt][2] = o[mt][nt][2] * fa0 + ob[(e++) * 32] * fb0;
+                o[mt][nt][3] = o[mt][nt][3] * fa1 + ob[(e++) * 32] * fb1;
+              }
+            }
+          }
+        }
+        named_bar_sync(1, NC * 32);
+      }
+      if (si == 0) {
+        const bool whole = (h.flags & kStartsUnit) && (h.flags & kEndsUnit);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float lt = l[nt][j];
+            lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+            const int col = nt * 8 + 2 * c + j;  // query head within the group
+            const float inv = 1.f / lt;
+            const float lse_v = (m[nt][j] + log2f(lt)) * kLn2;
+            if (col < G) {
+              const int qhl = hl * G + col;
+              if (whole) {
+                const int64_t qh = (int64_t)h.hg * HQU + qhl;
+                __nv_bfloat16* op = a.out + ((int64_t)h.b * a.num_q_heads + qh) * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                  op[mt * 16 + g] = __float2bfloat16_rn(o[mt][nt][j] * inv);
+                  op[mt * 16 + g + 8] = __float2bfloat16_rn(o[mt][nt][2 + j] * inv);
+                }
+                if (g == 0 && a.lse) a.lse[(int64_t)h.b * a.num_q_heads + qh] = lse_v;
+              } else {
+                float* pp = a.part_o + ((int64_t)h.part * HQU + qhl) * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                  pp[mt * 16 + g] = o[mt][nt][j] * inv;
+                  pp[mt * 16 + g + 8] = o[mt][nt][2 + j] * inv;
+                }
+                if (g == 0) a.part_lse[(int64_t)h.part * HQU + qhl] = lse_v;
+              }
+            }
+          }
+        }
+        if (warp == 0 && lane == 0) {
+          if (h.flags & kStartsUnit) a.unit_first[h.unit] = h.part;
+          if (h.flags & kEndsUnit) a.unit_last[h.unit] = h.part;
+        }
+      }
+    }
+    if (++stage == NS) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(288, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  const int NC = a.HC * a.W;
+  uint8_t* stages = smem;
+  const size_t stage_region = (size_t)NS * 2 * Ts * RS;
+  StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + stage_region);
+  uint64_t* full = reinterpret_cast<uint64_t*>(hdr + NS);
+  uint64_t* empty = full + NS;
+  float* mbuf = reinterpret_cast<float*>(empty + NS);
+
+  // rows that no copy writes (the tail of a partial slice) must hold finite values
+  for (size_t i = threadIdx.x; i < stage_region / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(stages)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5;
+  if (warp == NC) {
+    decode_producer<D>(a, stages, hdr, full, empty);
+  } else if (warp < NC) {
+    decode_consumer<D, NT>(a, stages, hdr, full, empty, mbuf);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Merge of the decode's split partials: one block per unit (request, head group).
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+  const int u = blockIdx.x;
+  const int b = u / a.nhg, hg = u % a.nhg;
+  const int HQU = a.HC * a.group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int VPL = D / 32;  // values per lane
+  const int L = __ldg(a.kv_lens + b);
+  if (L <= 0) {
+    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_LENGTH);
+    for (int qhl = warp; qhl < HQU; qhl += 4) {
+      const int64_t qh = (int64_t)hg * HQU + qhl;
+      __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) op[lane * VPL + i] = __float2bfloat16_rn(0.f);
+      if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = -INFINITY;
+    }
+    return;
+  }
+  const int first = a.unit_first[u], last = a.unit_last[u];
+  if (first == last) return;  // the decode kernel wrote this unit's output directly
+  if (first < 0 || last >= a.num_parts || last < first) {
+    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    return;
+  }
+  for (int qhl = warp; qhl < HQU; qhl += 4) {
+    float mx = -INFINITY;
+    for (int p = first; p <= last; ++p) mx = fmaxf(mx, a.part_lse[(int64_t)p * HQU + qhl]);
+    float acc[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+    float tot = 0.f;
+    for (int p = first; p <= last; ++p) {
+      const float w = __expf(a.part_lse[(int64_t)p * HQU + qhl] - mx);
+      tot += w;
+      const float* pp = a.part_o + ((int64_t)p * HQU + qhl) * D + lane * VPL;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) acc[i] += w * pp[i];
+    }
+    const float inv = 1.f / tot;
+    const int64_t qh = (int64_t)hg * HQU + qhl;
+    __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D + lane * VPL;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) op[i] = __float2bfloat16_rn(acc[i] * inv);
+    if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = mx + logf(tot);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Generic merge_states: one warp per (row, head).
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) merge_states_kernel(const float* __restrict__ o_parts,
+                                                           const float* __restrict__ lse_parts,
+                                                           int32_t S, int64_t rows_heads, int32_t D,
+                                                           __nv_bfloat16* __restrict__ out,
+                                                           float* __restrict__ lse) {
+  const int64_t rh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (rh >= rows_heads) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(lse_parts + (int64_t)s * rows_heads + rh));
+  __nv_bfloat16* op = out + rh * D;
+  if (mx == -INFINITY) {  // every split empty
+    for (int d = lane * 4; d < D; d += 128)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) op[d + i] = __float2bfloat16_rn(0.f);
+    if (lane == 0 && lse) lse[rh] = -INFINITY;
+    return;
+  }
+  float tot = 0.f;
+  for (int s = 0; s < S; ++s) tot += __expf(__ldg(lse_parts + (int64_t)s * rows_heads + rh) - mx);
+  const float inv = 1.f / tot;
+  for (int d = lane * 4; d < D; d += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float w = __expf(__ldg(lse_parts + (int64_t)s * rows_heads + rh) - mx);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * rows_heads + rh) * D + d));
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    op[d + 0] = __float2bfloat16_rn(acc.x * inv);
+    op[d + 1] = __float2bfloat16_rn(acc.y * inv);
+    op[d + 2] = __float2bfloat16_rn(acc.z * inv);
+    op[d + 3] = __float2bfloat16_rn(acc.w * inv);
+  }
+  if (lane == 0 && lse) lse[rh] = mx + logf(tot);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host-side planning
+// ---------------------------------------------------------------------------------------------
+struct DecodePlan {
+  int HC, nhg, W, G, NT, Ts, RS, NS;
+  size_t smem;
+  int ncta;
+  int64_t nunits, nparts;
+  size_t off_first, off_last, off_plse, off_po, ws_bytes;
+};
+
+constexpr size_t kSmemBudget = 225 * 1024;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return false;
+  if (D != 64 && D != 128) return false;
+  p.G = Hq / Hkv;
+  if (p.G > 16) return false;
+  p.NT = (p.G + 7) / 8;
+  p.HC = 1;
+  for (int d = 1; d <= 8; ++d)
+    if (Hkv % d == 0) p.HC = d;
+  p.nhg = Hkv / p.HC;
+  p.W = 8 / p.HC;
+  if (p.W < 1) p.W = 1;
+  p.Ts = 16 * p.W;
+  const int RB = p.HC * D * 2;
+  p.RS = RB + (((RB / 16) % 2 == 0) ? 16 : 0);
+  const size_t stage = (size_t)2 * p.Ts * p.RS;
+  const int mf = 4 * p.NT + (D / 16) * p.NT * 4;
+  const size_t mbytes = p.W > 1 ? (size_t)(p.W - 1) * p.HC * mf * 32 * 4 : 0;
+  const size_t fixed = mbytes + (size_t)kMaxStages * (sizeof(StageHdr) + 16);
+  if (fixed + 2 * stage > kSmemBudget) return false;
+  p.NS = (int)((kSmemBudget - fixed) / stage);
+  if (p.NS > kMaxStages) p.NS = kMaxStages;
+  p.smem = (size_t)p.NS * stage + (size_t)p.NS * (sizeof(StageHdr) + 16) + mbytes;
+  p.ncta = ncta;
+  p.nunits = (int64_t)B * p.nhg;
+  p.nparts = p.ncta + p.nunits;
+  const int HQU = p.HC * p.G;
+  p.off_first = 0;
+  p.off_last = align256(p.off_first + (size_t)p.nunits * 4);
+  p.off_plse = align256(p.off_last + (size_t)p.nunits * 4);
+  p.off_po = align256(p.off_plse + (size_t)p.nparts * HQU * 4);
+  p.ws_bytes = align256(p.off_po + (size_t)p.nparts * HQU * D * 4);
+  return true;
+}
+
+template <int D, int NT>
+pkv_status launch_decode(const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
+  auto kern = paged_decode_kernel<D, NT>;
+  static int configured_dev[64] = {0};
+  const int dev = pkv_host::current_device();
+  if (dev >= 0 && dev < 64 && configured_dev[dev] < (int)p.smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured_dev[dev] = (int)p.smem;
+  }
+  const int threads = (p.HC * p.W + 1) * 32;
+  kern<<<p.ncta, threads, p.smem, st>>>(a);
+  pkv_status s = pkv_host::launch_status();
+  if (s != PKV_OK) return s;
+  if (p.nunits > 0) {
+    decode_merge_kernel<D><<<(unsigned)p.nunits, 128, 0, st>>>(a);
+    s = pkv_host::launch_status();
+  }
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim) {
+  DecodePlan p;
+  const int n = pkv_host::sm_count();
+  if (n <= 0) return 0;
+  if (!make_plan(batch_size, num_q_heads, num_kv_heads, head_dim, n, p)) return 0;
+  return p.ws_bytes;
+}
+
+pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_size,
+                            int32_t num_q_heads, const int32_t* kv_indptr,
+                            const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            uint32_t* err_word, void* stream) {
+  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (batch_size == 0) return PKV_OK;
+  if (!q || !kv_indptr || !kv_indices || !kv_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (batch_size > 0x7fffffff / 64) return PKV_ERR_UNSUPPORTED;
+  const int D = pool->head_dim;
+  const int ncta = pkv_host::sm_count();
+  if (ncta <= 0) return PKV_ERR_CUDA;
+  DecodePlan p;
+  if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, D, ncta, p)) return PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < p.ws_bytes) return PKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+
+  DecodeArgs a;
+  a.k_pool = (const __nv_bfloat16*)pool->k;
+  a.v_pool = (const __nv_bfloat16*)pool->v;
+  a.num_pages = pool->num_pages;
+  a.page_size = pool->page_size;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = (const __nv_bfloat16*)q;
+  a.batch = batch_size;
+  a.num_q_heads = num_q_heads;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.kv_lens = kv_lens;
+  a.scale_log2 = sm_scale * pkv::kLog2e;
+  a.out = (__nv_bfloat16*)out;
+  a.lse = lse;
+  uint8_t* ws = (uint8_t*)workspace;
+  a.unit_first = (int32_t*)(ws + p.off_first);
+  a.unit_last = (int32_t*)(ws + p.off_last);
+  a.part_lse = (float*)(ws + p.off_plse);
+  a.part_o = (float*)(ws + p.off_po);
+  a.err_word = err_word;
+  a.HC = p.HC;
+  a.nhg = p.nhg;
+  a.W = p.W;
+  a.group = p.G;
+  a.row_stride = p.RS;
+  a.stage_tokens = p.Ts;
+  a.num_stages = p.NS;
+  a.num_parts = (int32_t)p.nparts;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  if (D == 128) {
+    return p.NT == 1 ? launch_decode<128, 1>(p, a, st) : launch_decode<128, 2>(p, a, st);
+  }
+  return p.NT == 1 ? launch_decode<64, 1>(p, a, st) : launch_decode<64, 2>(p, a, st);
+}
+
+pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
+                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                            float* lse, void* stream) {
+  if (num_splits < 0 || num_rows < 0 || num_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
+  if (num_rows == 0) return PKV_OK;
+  if (!o_parts || !lse_parts || !out || num_splits == 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim % 4 != 0 || head_dim > 512) return PKV_ERR_UNSUPPORTED;
+  if (!pkv_host::aligned16(o_parts)) return PKV_ERR_INVALID_ARG;
+  const int64_t rh = (int64_t)num_rows * num_heads;
+  const int warps = 8;
+  const int64_t blocks = (rh + warps - 1) / warps;
+  if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  merge_states_kernel<<<(unsigned)blocks, warps * 32, 0, (cudaStream_t)stream>>>(
+      o_parts, lse_parts, num_splits, rh, head_dim, (__nv_bfloat16*)out, lse);
+  return pkv_host::launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,494 @@
+// Ragged extend attention (prefill / chunked prefill over a cached prefix) on tcgen05 tensor cores.
+//
+// What it computes: request b's E_b new tokens attend causally to its KV, read in place from the
+// paged pool; query i sits at absolute position P_b + i and sees positions j <= P_b + i (the
+// causal mask offset by the cached prefix, Mini-SGLang README "Reference Attention Backends",
+// torch backend), with GQA (query head h reads KV head h / G) and prefix pages that several
+// requests share (mini-sglang README, "KVcache Management": Radix Attention).  Chunked prefill
+// (nanoLLMServe README, "v0.7 Chunked Prefill") is the same call with a non-zero prefix.
+//
+// Design for GB300:
+//  * One CTA per (128-row Q tile, KV head, request).  The 128 rows are (token, group head) pairs:
+//    128/G consecutive tokens times the G query heads that share the KV head, so each K/V tile
+//    loaded is used by the whole group.  Q arrives by one 3-D TMA box per 64-column half.
+//  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
+//    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
+//  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=2x64, K=64) run as tcgen05.mma issued
+//    by one thread, accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.
+//  * Four softmax warps own one row each per thread: they read S from TMEM, apply the causal
+//    mask and the online softmax in fp32 (the running max is only moved when it grows by more
+//    than 2^8, so O is rescaled in TMEM rarely), write P as bf16 into shared memory in the
+//    swizzled K-major layout the PV MMA reads, and finally normalise O and store it.
+//  * Two CTAs fit on an SM (112 KB of shared memory and 256 TMEM columns each), so one CTA's
+//    softmax overlaps the other's MMAs.
+#include <cudaTypedefs.h>
+
+#include "tc05.cuh"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
+constexpr int kBN = 64;   // KV positions per tile
+constexpr int kHD = 128;  // head_dim
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 256); S buffers at [0,64) and [64,128)
+
+constexpr uint32_t kQBytes = kBM * kHD * 2;  // 32 KB, two 64-column halves
+constexpr uint32_t kQHalf = kQBytes / 2;
+constexpr uint32_t kKVHalf = kBN * 128;      // 64 positions x 64 dims, 8 KB
+constexpr uint32_t kKVStage = 2 * kKVHalf;   // 16 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
+constexpr uint32_t kOffP = kOffV + 2 * kKVStage;
+constexpr uint32_t kPBytes = kBM * kBN * 2;  // 16 KB
+constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
+  uint32_t tmem_base;
+  uint32_t pad;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct ExtendArgs {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* prefix_lens;
+  __nv_bfloat16* out;
+  float* lse;
+  uint32_t* err_word;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t log2_ps;
+  int32_t num_q_heads;
+  int32_t group;
+  int32_t log2_group;
+  int32_t tokens_per_tile;
+  float scale_log2;
+};
+
+struct Work {
+  int h, b, qo0, E, t0, P, L, kv_end, n_tiles;
+};
+
+// TMA row coordinate of box i of KV tile j, or -1 when the box is not loaded.
+__device__ __forceinline__ int kv_box_row(const ExtendArgs& a, const Work& w, int p0, int np, int j,
+                                          int i, int R, bool report_errors) {
+  const int pos0 = j * kBN + i * R;
+  if (pos0 >= w.kv_end) return -1;
+  const int pidx = pos0 >> a.log2_ps;
+  if (pidx >= np) {
+    if (report_errors) report(a.err_word, PKV_DEVERR_LENGTH);
+    return -1;
+  }
+  const int64_t page = __ldg(a.kv_indices + p0 + pidx);
+  if (page < 0 || page >= a.num_pages) {
+    if (report_errors) report(a.err_word, PKV_DEVERR_PAGE_OOB);
+    return -1;
+  }
+  return (int)(page * a.page_size + (pos0 & (a.page_size - 1)));
+}
+
+__device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w) {
+  const int G = a.group;
+  mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+  tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.qo0 + w.t0, &bars->q_full);
+  tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.qo0 + w.t0, &bars->q_full);
+  const int p0 = __ldg(a.kv_indptr + w.b);
+  const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
+  const int R = min(a.page_size, kBN);
+  const int nbox = kBN / R;
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    const uint32_t ph = (j >> 1) & 1;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+      uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
+      const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
+      if (!mbar_wait(empty, ph ^ 1)) {
+        report(a.err_word, PKV_DEVERR_TIMEOUT);
+        return false;
+      }
+      int nload = 0;
+      for (int i = 0; i < nbox; ++i) nload += kv_box_row(a, w, p0, np, j, i, R, false) >= 0;
+      mbar_arrive_expect_tx(full, (uint32_t)nload * R * 128 * 2);
+      const uint32_t base = sb + (kv ? kOffV : kOffK) + st * kKVStage;
+      for (int i = 0; i < nbox; ++i) {
+        const int z = kv_box_row(a, w, p0, np, j, i, R, kv == 0);
+        if (z < 0) continue;
+        const uint32_t dst = base + i * R * 128;
+        tma_load_3d(dst, tm, 0, w.h, z, full);
+        tma_load_3d(dst + kKVHalf, tm, 64, w.h, z, full);
+      }
+    }
+  }
+  return true;
+}
+
+__device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
+  constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
+  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, 64, true);
+  if (!mbar_wait(&bars->q_full, 0)) return false;
+  auto issue_pv = [&](int t) -> bool {
+    const int st = t & 1;
+    if (!mbar_wait(&bars->p_full, t & 1)) return false;
+    if (!mbar_wait(&bars->v_full[st], (t >> 1) & 1)) return false;
+    tc_fence_after();
+    const uint32_t vb = sb + kOffV + st * kKVStage;
+#pragma unroll
+    for (int ks = 0; ks < kBN / 16; ++ks) {
+      const uint64_t adesc = smem_desc_sw128(sb + kOffP + ks * 32, 16, 1024);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint64_t bdesc = smem_desc_sw128(vb + half * kKVHalf + ks * 2048, 1024, 1024);
+        umma_ss(tmem + kColO + half * 64, adesc, bdesc, idesc_pv, t > 0 || ks > 0);
+      }
+    }
+    umma_commit(&bars->pv_done);
+    umma_commit(&bars->v_empty[st]);
+    return true;
+  };
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    if (!mbar_wait(&bars->k_full[st], (j >> 1) & 1)) return false;
+    if (!mbar_wait(&bars->s_free[st], ((j >> 1) & 1) ^ 1)) return false;
+    tc_fence_after();
+    const uint32_t kb = sb + kOffK + st * kKVStage;
+#pragma unroll
+    for (int ks = 0; ks < kHD / 16; ++ks) {
+      const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+      const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+      umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
+    }
+    umma_commit(&bars->s_full[st]);
+    umma_commit(&bars->k_empty[st]);
+    if (j > 0 && !issue_pv(j - 1)) return false;
+  }
+  return issue_pv(w.n_tiles - 1);
+}
+
+__device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, uint32_t tmem,
+                               const Work& w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;        // TMEM lane quadrant this warp may access
+  const int r = wq * 32 + lane;   // tile row == TMEM lane
+  const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
+  const int G = a.group;
+  const int tok = w.t0 + (r >> a.log2_group);
+  const int g = r & (G - 1);
+  const bool valid = tok < w.E;
+  const int limit = min(w.P + tok, w.L - 1);  // last visible KV position of this row
+  const int min_limit = w.P + w.t0;            // smallest limit over the tile's rows
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[st], (j >> 1) & 1));
+    if (!ok) break;
+    tc_fence_after();
+    float s[64];
+    {
+      float lo[32], hi[32];
+      tmem_ld32(taddr + st * 64, lo);
+      tmem_ld32(taddr + st * 64 + 32, hi);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = lo[c];
+        s[32 + c] = hi[c];
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->s_free[st]);
+
+    const int pos0 = j * kBN;
+    float mx = -INFINITY;
+    if (pos0 + kBN - 1 <= min_limit) {
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        s[c] *= a.scale_log2;
+        mx = fmaxf(mx, s[c]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        s[c] = (pos0 + c <= limit) ? s[c] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+    }
+    const float m_new = fmaxf(m_used, mx);
+    const bool resc = m_new > m_used + 8.f;  // always true on the first tile (m_used = -inf)
+    const float m_ref = resc ? m_new : m_used;
+    const float corr = resc ? ex2(m_used - m_ref) : 1.f;
+    uint32_t pk[kBN / 2];
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kBN / 2; ++c) {
+      const float p0 = ex2(s[2 * c] - m_ref), p1 = ex2(s[2 * c + 1] - m_ref);
+      sum += p0 + p1;
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    l = l * corr + sum;
+    m_used = m_ref;
+
+    if (j > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (j - 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int ch = 0; ch < kHD / 32; ++ch) {
+          float o[32];
+          tmem_ld32(taddr + kColO + ch * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(taddr + kColO + ch * 32, o);
+        }
+        tmem_wait_st();
+      }
+    }
+    if (j == w.n_tiles - 1 && w.kv_end < pos0 + kBN) {
+      // V rows past the last needed position hold stale or unused-slot data; zero them so that
+      // P = 0 times V stays 0 in the PV MMA.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j >> 1) & 1));
+      if (!ok) break;
+      const int r0 = w.kv_end - pos0;
+      const int nchunks = (kBN - r0) * 8 * 2;  // rows x 16-byte chunks x halves
+      uint8_t* vb = smem + kOffV + st * kKVStage;
+      for (int idx = r; idx < nchunks; idx += kBM) {
+        const int half = idx & 1, rc = idx >> 1;
+        const int row = r0 + (rc >> 3), ch = rc & 7;
+        *reinterpret_cast<uint4*>(vb + half * kKVHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    uint8_t* prow = smem + kOffP + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_full);
+  }
+
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (w.n_tiles - 1) & 1));
+  if (!ok) {
+    if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    return;
+  }
+  tc_fence_after();
+  const float inv = 1.f / l;
+  const int64_t row = (int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g;
+  uint4* orow = reinterpret_cast<uint4*>(a.out + row * kHD);
+#pragma unroll 1
+  for (int ch = 0; ch < kHD / 32; ++ch) {
+    float o[32];
+    tmem_ld32(taddr + kColO + ch * 32, o);
+    tmem_wait_ld();
+    if (valid) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        orow[ch * 4 + q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                      pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                      pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                      pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+    }
+  }
+  if (valid && a.lse) a.lse[row] = (m_used + log2f(l)) * kLn2;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Work w;
+  w.t0 = blockIdx.x * a.tokens_per_tile;
+  w.h = blockIdx.y;
+  w.b = blockIdx.z;
+  w.qo0 = __ldg(a.qo_indptr + w.b);
+  w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
+  if (w.t0 >= w.E) return;  // uniform: this tile has no rows
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_INTERNAL);
+    return;
+  }
+  w.P = __ldg(a.prefix_lens + w.b);
+  w.L = w.P + w.E;
+  w.kv_end = w.P + min(w.t0 + a.tokens_per_tile, w.E);
+  w.n_tiles = (w.kv_end + kBN - 1) / kBN;
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 4);
+    }
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->pv_done, 1);
+    fence_mbar_init();
+    prefetch_tmap(&a.tm_q);
+    prefetch_tmap(&a.tm_k);
+    prefetch_tmap(&a.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && !extend_producer(a, sb, bars, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+  } else if (warp == 1) {
+    if (lane == 0 && !extend_mma(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    __syncwarp();
+  } else {
+    extend_softmax(a, smem, bars, tmem, w);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host
+// ---------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+               uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int log2_exact(int x) {
+  if (x <= 0 || (x & (x - 1))) return -1;
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_extend_len) {
+  (void)batch_size;
+  (void)num_q_heads;
+  (void)num_kv_heads;
+  (void)head_dim;
+  (void)max_extend_len;
+  return 0;
+}
+
+pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
+                            const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
+                            const int32_t* kv_indptr, const int32_t* kv_indices,
+                            const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            uint32_t* err_word, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || num_q_tokens < 0 ||
+      max_extend_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch_size == 0 || num_q_tokens == 0 || max_extend_len == 0) return PKV_OK;
+  if (!q || !qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (pool->head_dim != kHD) return PKV_ERR_UNSUPPORTED;
+  const int G = num_q_heads / pool->num_kv_heads;
+  const int lg = log2_exact(G);
+  const int lps = log2_exact(pool->page_size);
+  // page boxes of at least 8 rows keep every TMA destination on a 1024-byte swizzle atom
+  if (lg < 0 || G > 16 || lps < 3) return PKV_ERR_UNSUPPORTED;
+  if (pool->num_pages * (int64_t)pool->page_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (batch_size > 65535 || pool->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+
+  ExtendArgs a;
+  const int tpt = kBM / G;
+  const uint64_t Hq = num_q_heads, Hkv = pool->num_kv_heads;
+  const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
+  const uint32_t R = pool->page_size < kBN ? pool->page_size : kBN;
+  if (!encode_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_tokens, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
+      !encode_3d(&a.tm_k, pool->k, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R) ||
+      !encode_3d(&a.tm_v, pool->v, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R))
+    return PKV_ERR_CUDA;
+  a.qo_indptr = qo_indptr;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.prefix_lens = prefix_lens;
+  a.out = (__nv_bfloat16*)out;
+  a.lse = lse;
+  a.err_word = err_word;
+  a.num_pages = pool->num_pages;
+  a.page_size = pool->page_size;
+  a.log2_ps = lps;
+  a.num_q_heads = num_q_heads;
+  a.group = G;
+  a.log2_group = lg;
+  a.tokens_per_tile = tpt;
+  a.scale_log2 = sm_scale * kLog2e;
+
+  static bool configured[64] = {false};
+  const int dev = pkv_host::current_device();
+  if (dev < 0) return PKV_ERR_CUDA;
+  if (dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(paged_extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) configured[dev] = true;
+  }
+  const int tiles = (max_extend_len + tpt - 1) / tpt;
+  dim3 grid(tiles, pool->num_kv_heads, batch_size);
+  paged_extend_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(a);
+  return pkv_host::launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+"""Ragged extend (tcgen05) on the GPU against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import random_small_batch
+from _fixtures import golden_tensors, load_golden
+from _gpu_helpers import DeviceBatch, assert_attention_close, config_with_append
+
+pytestmark = pytest.mark.gpu
+
+
+def run_extend(lib, b, kp, vp, **kw):
+    dev = "cuda"
+    return lib.paged_extend(b.ext_q.to(dev), kp.to(dev), vp.to(dev), b.ext_qo_indptr.to(dev),
+                            b.ext_kv_indptr.to(dev), b.ext_kv_indices.to(dev),
+                            b.ext_prefix_lens.to(dev), b.max_extend_len, b.sm_scale, **kw)
+
+
+def oracle_extend(b, kp, vp, **kw):
+    return oracle.paged_extend(b.ext_q, kp, vp, b.ext_qo_indptr, b.ext_kv_indptr, b.ext_kv_indices,
+                               b.ext_prefix_lens, b.page_size, b.sm_scale, **kw)
+
+
+def test_golden_extend_on_gpu(lib):
+    c = load_golden()["extend_prefix_offset_uniform"]
+    t = golden_tensors(c)
+    D = 128
+
+    def pad(x):
+        y = torch.zeros(x.shape[:-1] + (D,), dtype=x.dtype)
+        y[..., : x.shape[-1]] = x
+        return y
+
+    out, lse = lib.paged_extend(pad(t["q"]).cuda(), pad(t["k_pool"]).cuda(), pad(t["v_pool"]).cuda(),
+                                t["qo_indptr"].cuda(), t["kv_indptr"].cuda(), t["kv_indices"].cuda(),
+                                t["prefix_lens"].cuda(), 2, c["sm_scale"])
+    o = out.float().cpu().numpy()
+    assert np.abs(o[..., :2] - np.array(c["expect_o"])).max() <= 1e-2
+    assert np.all(o[..., 2:] == 0)
+    assert np.abs(lse.cpu().numpy() - np.array(c["expect_lse"])).max() <= 1e-3
+
+
+def test_extend_radix_prefix_workload(lib):
+    b, kp, vp = config_with_append(3)
+    d = DeviceBatch(b)
+    lib.kv_append(d.k_pool, d.v_pool, d.k_new, d.v_new, d.slot_mapping)
+    out, lse = run_extend(lib, b, d.k_pool, d.v_pool)
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what="config 3")
+
+
+@pytest.mark.slow
+def test_extend_mixed_step_chunks(lib):
+    b, kp, vp = config_with_append(5)
+    d = DeviceBatch(b)
+    lib.kv_append(d.k_pool, d.v_pool, d.k_new, d.v_new, d.slot_mapping)
+    out, lse = run_extend(lib, b, d.k_pool, d.v_pool)
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what="config 5 extends")
+
+
+CASES = [
+    # (page_size, Hq, Hkv, [(prefix, extend), ...])
+    (16, 32, 8, [(0, 1), (0, 5), (3, 40), (100, 33), (700, 129)]),
+    (16, 8, 8, [(0, 128), (5, 200), (64, 64)]),
+    (8, 16, 2, [(7, 31), (0, 64)]),
+    (64, 32, 4, [(63, 65), (128, 1), (0, 300)]),
+    (128, 16, 1, [(5, 130), (250, 10)]),
+    (256, 16, 16, [(300, 100)]),
+    (16, 32, 2, [(31, 17), (0, 9)]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"ps{c[0]}-q{c[1]}-kv{c[2]}" for c in CASES])
+def test_extend_property_sweep(lib, case):
+    ps, hq, hkv, ext = case
+    b = random_small_batch(200 + ps + hq, page_size=ps, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                           extend=ext)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, ps)
+    out, lse = run_extend(lib, b, kp, vp)
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what=str(case))
+
+
+def test_extend_shared_prefix_pages(lib):
+    b = random_small_batch(17, page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                           extend=[(512, 100), (600, 37), (1000, 256), (40, 50)], share_extend_prefix=512)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    out, lse = run_extend(lib, b, kp, vp)
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what="shared prefix")
+
+
+def test_extend_is_deterministic_and_matches_decode(lib):
+    b = random_small_batch(18, page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                           decode_lens=(77, 500, 1031), extend=[(300, 70)])
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    kpd, vpd = kp.cuda(), vp.cuda()
+    o1, l1 = run_extend(lib, b, kpd, vpd)
+    o2, l2 = run_extend(lib, b, kpd, vpd)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    # decode requests viewed as one-token extends give the decode result (within tolerance)
+    B = b.num_decode
+    qo = torch.arange(B + 1, dtype=torch.int32).cuda()
+    eo, el = lib.paged_extend(b.dec_q.cuda(), kpd, vpd, qo, b.dec_kv_indptr.cuda(), b.dec_kv_indices.cuda(),
+                              (b.dec_kv_lens - 1).cuda(), 1, b.sm_scale)
+    do, dl = lib.paged_decode(b.dec_q.cuda(), kpd, vpd, b.dec_kv_indptr.cuda(), b.dec_kv_indices.cuda(),
+                              b.dec_kv_lens.cuda(), b.sm_scale)
+    assert (eo.float() - do.float()).abs().max().item() <= 2e-2
+    assert (el - dl).abs().max().item() <= 1e-3
+
+
+def test_extend_bad_page_index_is_reported(lib):
+    b = random_small_batch(19, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(40, 30)])
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    ind = b.ext_kv_indices.clone()
+    ind[1] = b.num_pages + 3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.paged_extend(b.ext_q.cuda(), kp.cuda(), vp.cuda(), b.ext_qo_indptr.cuda(), b.ext_kv_indptr.cuda(),
+                     ind.cuda(), b.ext_prefix_lens.cuda(), b.max_extend_len, b.sm_scale, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lib.DEVERR_PAGE_OOB
+
+
+def test_extend_host_checks(lib):
+    b = random_small_batch(20, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=64, extend=[(4, 4)])
+    with pytest.raises(lib.PagedKVError) as e:
+        run_extend(lib, b, b.k_pool, b.v_pool)
+    assert e.value.status == 2  # head_dim 64 not built for extend
+    b = random_small_batch(21, page_size=24, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
+    with pytest.raises(lib.PagedKVError) as e:
+        run_extend(lib, b, b.k_pool, b.v_pool)
+    assert e.value.status == 2  # page size not a power of two
+    b = random_small_batch(23, page_size=4, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
+    with pytest.raises(lib.PagedKVError) as e:
+        run_extend(lib, b, b.k_pool, b.v_pool)
+    assert e.value.status == 2  # pages smaller than 8 rows
+    b = random_small_batch(22, page_size=16, num_q_heads=6, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
+    with pytest.raises(lib.PagedKVError) as e:
+        run_extend(lib, b, b.k_pool, b.v_pool)
+    assert e.value.status == 2  # group size 3
