@@ -53,6 +53,18 @@ def _dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank timings (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 # ---------------------------------------------------------------------------------------------
 # algorithmic work of the workload (from the generated lengths)
 # ---------------------------------------------------------------------------------------------
@@ -290,10 +302,7 @@ def run_ours(args, ws, rank, local):
     e2e_ms = s2.elapsed_time(e2)
 
     # ---- max over ranks --------------------------------------------------------------------
-    vals = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = float(vals[0]), float(vals[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dev)
 
     peaks = _peaks()
     ms_step = elapsed_ms / K

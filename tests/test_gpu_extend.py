@@ -24,6 +24,27 @@ def oracle_extend(b, kp, vp, **kw):
                                b.ext_prefix_lens, b.page_size, b.sm_scale, **kw)
 
 
+def _repage(pool, indptr, indices, lens, ps, new_ps):
+    """The same requests' rows laid out in a fresh NaN-filled pool of page size new_ps, pages in
+    reverse order (a test-side re-layout: position j of request b -> page j // new_ps)."""
+    B = len(lens)
+    need = [-(-int(L) // new_ps) for L in lens]
+    n = sum(need) + 1
+    out = torch.full((n, new_ps) + tuple(pool.shape[2:]), float("nan"), dtype=pool.dtype)
+    new_ind, new_ptr, nxt = [], [0], n - 1
+    for b in range(B):
+        pages = []
+        for _ in range(need[b]):
+            pages.append(nxt)
+            nxt -= 1
+        for j in range(int(lens[b])):
+            src = pool[indices[indptr[b] + j // ps], j % ps]
+            out[pages[j // new_ps], j % new_ps] = src
+        new_ind += pages
+        new_ptr.append(len(new_ind))
+    return out, torch.tensor(new_ptr, dtype=torch.int32), torch.tensor(new_ind, dtype=torch.int32)
+
+
 def test_golden_extend_on_gpu(lib):
     c = load_golden()["extend_prefix_offset_uniform"]
     t = golden_tensors(c)
@@ -34,9 +55,12 @@ def test_golden_extend_on_gpu(lib):
         y[..., : x.shape[-1]] = x
         return y
 
-    out, lse = lib.paged_extend(pad(t["q"]).cuda(), pad(t["k_pool"]).cuda(), pad(t["v_pool"]).cuda(),
-                                t["qo_indptr"].cuda(), t["kv_indptr"].cuda(), t["kv_indices"].cuda(),
-                                t["prefix_lens"].cuda(), 2, c["sm_scale"])
+    lens = (t["prefix_lens"] + t["qo_indptr"][1:] - t["qo_indptr"][:-1]).tolist()
+    ind, idx = t["kv_indptr"].tolist(), t["kv_indices"].tolist()
+    kp, ptr, new_idx = _repage(pad(t["k_pool"]), ind, idx, lens, c["page_size"], 8)
+    vp, _, _ = _repage(pad(t["v_pool"]), ind, idx, lens, c["page_size"], 8)
+    out, lse = lib.paged_extend(pad(t["q"]).cuda(), kp.cuda(), vp.cuda(), t["qo_indptr"].cuda(),
+                                ptr.cuda(), new_idx.cuda(), t["prefix_lens"].cuda(), 2, c["sm_scale"])
     o = out.float().cpu().numpy()
     assert np.abs(o[..., :2] - np.array(c["expect_o"])).max() <= 1e-2
     assert np.all(o[..., 2:] == 0)
