@@ -195,7 +195,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkv.load()
-    b = make_config(WORKLOAD_IDX)
+    b = load_workload(args.workload)
     counts = workload_counts(b)
     st = torch.cuda.Stream(device=dev)
 
@@ -215,18 +215,25 @@ def run_ours(args, ws, rank, local):
     dws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     max_e = b.max_extend_len
 
+    do_app = args.op in ("all", "append")
+    do_dec = args.op in ("all", "decode") and b.num_decode > 0
+    do_ext = args.op in ("all", "extend") and b.num_extend > 0
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(st)
-        pkv.kv_append(kp, vp, kn, vn, sm, stream=st)
+        if do_app:
+            pkv.kv_append(kp, vp, kn, vn, sm, stream=st)
         if ev is not None:
             ev[1].record(st)
-        pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
-                         workspace=dws, stream=st)
+        if do_dec:
+            pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
+                             workspace=dws, stream=st)
         if ev is not None:
             ev[2].record(st)
-        pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
-                         lse=e_lse, stream=st)
+        if do_ext:
+            pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
+                             lse=e_lse, stream=st)
         if ev is not None:
             ev[3].record(st)
 
@@ -285,7 +292,7 @@ def run_ours(args, ws, rank, local):
         for n, t in host_out.items():
             t.copy_(dev_out[n], non_blocking=True)
 
-    K2 = max(1, min(K, 200))
+    K2 = max(1, min(K, 200)) if not args.no_e2e else 1
     with torch.cuda.stream(st):
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -360,7 +367,7 @@ def run_ours(args, ws, rank, local):
         },
         "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 4 * K,
+        "gpu_launches": (int(do_app) + 2 * int(do_dec) + int(do_ext)) * K,
         "clocks": clk,
     }
     return line
@@ -448,8 +455,26 @@ def run_reference(args, ws, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+def load_workload(name):
+    """The mixed step (default), or a few-hundred-MB case for profiler captures."""
+    if name == "mixed":
+        from workloads import make_config
+
+        return make_config(WORKLOAD_IDX)
+    if name == "profile":
+        from workloads import random_small_batch
+
+        return random_small_batch(7001, page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                  decode_lens=(4096,) * 16, decode_new=1,
+                                  extend=((1024, 512), (1536, 512)), pool_slack=1.1)
+    raise ValueError(name)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="mixed", choices=["mixed", "profile"])
+    ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"])
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
@@ -474,9 +499,7 @@ def main():
     line = run_ours(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            from workloads import make_config
-
-            line["cpu_baseline"] = cpu_baseline(make_config(WORKLOAD_IDX), args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(load_workload(args.workload), args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
