@@ -126,6 +126,30 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
                             uint32_t* err_word, void* stream);
 
 /*
+ * Decode for callers that cannot allocate device memory.  No counterpart on the pages: this is a
+ * convenience of this library.  A serving engine that reserves a fixed share of HBM for its KV
+ * pool, or code that must not call cudaMalloc (and take its implicit device synchronisation) in
+ * the middle of a step, has no workspace to pass to pkv_paged_decode.  This entry point takes the
+ * same arguments minus the workspace and uses a scratch array that the library holds in device
+ * memory: PKV_DECODE_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, until the
+ * process exits.  It allocates nothing itself.
+ *   - Shapes whose pkv_decode_workspace_size() exceeds PKV_DECODE_NOALLOC_SCRATCH_BYTES are
+ *     rejected with PKV_ERR_WORKSPACE (Hq=32, head_dim 128 fits about 800 requests).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, which
+ *     may load the module on that device); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents; nothing in it needs
+ *     to start at zero.  Calls that can overlap on the GPU (different streams without ordering)
+ *     race on it: serialise them.
+ * Results are those of pkv_paged_decode with the same arguments.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+pkv_status pkv_paged_decode_noalloc(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                    int32_t num_q_heads, const int32_t* kv_indptr,
+                                    const int32_t* kv_indices, const int32_t* kv_lens,
+                                    float sm_scale, void* out, float* lse, uint32_t* err_word,
+                                    void* stream);
+
+/*
  * Bytes of workspace pkv_paged_extend needs (0 when none is needed).
  */
 size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,

@@ -22,6 +22,8 @@
 //    by movmatrix.  KV is read exactly once per CTA per token, for all heads of the group.
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -731,3 +733,63 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Decode without a caller-supplied workspace.
+//
+// Some callers cannot allocate device memory when they need a decode: a serving engine that
+// reserves a fixed share of HBM for its KV pool up front leaves nothing for per-call buffers,
+// and code that must not take cudaMalloc's implicit device-wide synchronisation (or its failure
+// modes) in the middle of a step has no safe place to get a workspace either.  For them the
+// split partials live in one file-scope device array, sized once, held by every GPU that loads
+// this library for as long as the process lives.
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_decode_scratch[PKV_DECODE_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+// Device address of g_decode_scratch on the current device (looked up once per device; in host
+// code the array's name is only a stand-in for the symbol, never a device pointer).
+void* scratch_on_current_device() {
+  const int dev = pkv_host::current_device();
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_paged_decode_noalloc(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                               int32_t num_q_heads, const int32_t* kv_indptr,
+                                               const int32_t* kv_indices, const int32_t* kv_lens,
+                                               float sm_scale, void* out, float* lse,
+                                               uint32_t* err_word, void* stream) {
+  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (batch_size == 0) return PKV_OK;
+  const int n = pkv_host::sm_count();
+  if (n <= 0) return PKV_ERR_CUDA;
+  DecodePlan p;
+  if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, pool->head_dim, n, p)) {
+    // let the regular entry point classify the shape error
+    return pkv_paged_decode(pool, q, batch_size, num_q_heads, kv_indptr, kv_indices, kv_lens,
+                            sm_scale, out, lse, nullptr, 0, err_word, stream);
+  }
+  if (p.ws_bytes > (size_t)PKV_DECODE_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  void* ws = scratch_on_current_device();
+  if (!ws) return PKV_ERR_CUDA;
+  // The partials need no initial contents: every slot a merge reads is written earlier in the
+  // same call.  Calls that overlap on the GPU (other streams) share the array and race.
+  return pkv_paged_decode(pool, q, batch_size, num_q_heads, kv_indptr, kv_indices, kv_lens, sm_scale,
+                          out, lse, ws, (size_t)PKV_DECODE_NOALLOC_SCRATCH_BYTES, err_word, stream);
+}
