@@ -173,15 +173,23 @@ def _kernel_hash():
 
 
 def _traffic_record():
-    """DRAM bytes per decode launch from the committed ncu summary, if taken on this source."""
-    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    """DRAM bytes per decode launch from the committed ncu summary of the mixed step, if that
+    capture was taken on the current decode source (its hash is recorded beside the figure)."""
+    p = os.path.join(ROOT, "profiles", "paged_decode_mixed_step_dram.md")
     if not os.path.exists(p):
         return None
+    fields = {}
     with open(p) as f:
-        d = json.load(f)
-    if d.get("source_hash") != _kernel_hash():
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                k, v = line[2:].split(": ", 1)
+                fields[k.strip("` ")] = v.strip().strip("`")
+    if fields.get("source_hash") != _kernel_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def run_ours(args, ws, rank, local):

@@ -7,24 +7,27 @@
 // the Triton decode kernel).  Long requests are split and merged by log-sum-exp (flash-decoding).
 //
 // Design for GB300 (HBM-bound: ~2-8 flop per KV byte):
-//  * Persistent grid, one CTA per SM.  The KV of all (request, KV-head-group) units forms one
-//    token stream; every CTA takes an equal contiguous share of it, so work is balanced whatever
-//    the length mix, and a unit cut by a share boundary leaves one partial per CTA that touched
-//    it (merged by a second kernel).  A CTA covers HC KV heads so that one token row of the CTA
-//    is a single contiguous HC*D*2-byte run of the NHD page.
-//  * One producer warp walks the CTA's share and streams token rows with cp.async.bulk into a
-//    ring of NS shared-memory stages (K and V), completion counted in bytes on an mbarrier.
-//    Rows land at a padded stride so the warps' ldmatrix reads are bank-conflict free.
+//  * Persistent grid, one CTA per SM.  The KV of all (request, KV-head-group) units, cut into
+//    16-token slices counted from each unit's first position, forms one stream; every CTA takes an
+//    equal contiguous share of slices, so work is balanced whatever the length mix.  A unit cut by
+//    a share boundary leaves one partial per CTA that touched it, merged by a second kernel.  A CTA
+//    covers HC KV heads, so one token row of the CTA is a single contiguous HC*D*2-byte run.
+//  * One producer warp walks the share and fills a ring of shared-memory stages, completion
+//    counted in bytes on mbarriers.  When the page size is a multiple of 16 a 16-token slice lies
+//    in one page and is fetched by TMA as one 3-D box per 64-dim half, [64 dims x 16 rows x HC
+//    heads] with 128-byte swizzle: each head's slice lands as its own 2 KB block whose rows are
+//    swizzled, so the warps' ldmatrix reads are conflict free.  Other page sizes use one
+//    cp.async.bulk per token row, into rows padded to a conflict-free stride.
 //  * Consumer warps (one per KV head, W per head when HC < 8) take 16-token slices.  Scores are
 //    computed transposed, S^T = K Q^T, with m16n8k16 bf16 MMAs (tokens fill M=16, the G query
 //    heads of the group fill N=8, so nothing is padded to 16 heads); the online softmax keeps a
-//    running max and sum in fp32 per head; P^T is turned into the B operand of O^T += V^T P^T
-//    by movmatrix.  KV is read exactly once per CTA per token, for all heads of the group.
+//    running max and sum in fp32 per head; P^T is turned into the B operand of O^T += V^T P^T by
+//    movmatrix.  KV is read exactly once per CTA per token, for all heads of the group.
 #include <float.h>
 
 #include <mutex>
 
-#include "common.cuh"
+#include "tc05.cuh"
 
 namespace {
 
@@ -47,6 +50,8 @@ struct StageHdr {
 };
 
 struct DecodeArgs {
+  CUtensorMap tm_k;  // pool as (dim, row, head), box [64 x 16 x HC]; used when use_tma
+  CUtensorMap tm_v;
   const __nv_bfloat16* k_pool;
   const __nv_bfloat16* v_pool;
   int64_t num_pages;
@@ -66,14 +71,15 @@ struct DecodeArgs {
   int32_t* unit_first;
   int32_t* unit_last;
   uint32_t* err_word;
-  int32_t HC;       // KV heads per CTA
-  int32_t nhg;      // head groups = num_kv_heads / HC
-  int32_t W;        // consumer warps per KV head
-  int32_t group;    // query heads per KV head
-  int32_t row_stride;    // shared-memory bytes per token row
+  int32_t HC;            // KV heads per CTA
+  int32_t nhg;           // head groups = num_kv_heads / HC
+  int32_t W;             // consumer warps per KV head
+  int32_t group;         // query heads per KV head
+  int32_t row_stride;    // shared-memory bytes per token row (row-copy layout)
   int32_t stage_tokens;  // tokens per stage = 16 * W
   int32_t num_stages;
   int32_t num_parts;     // partial slots in the workspace
+  uint32_t kv_region;    // bytes of the K (or V) part of one stage
 };
 
 constexpr int kMaxStages = 8;
@@ -86,30 +92,52 @@ struct Consumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// Producer: walk the CTA's share of the token stream and fill stages.
+// Producer: walk the CTA's share of the slice stream and fill stages.
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool TMA>
 __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* hdr,
                                 uint64_t* full, uint64_t* empty) {
   const int lane = threadIdx.x & 31;
-  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride, W = a.W;
   const int nhg = a.nhg;
+  const int ps = a.page_size;
   const uint32_t RB = (uint32_t)a.HC * D * 2;
   const int64_t row_elems = (int64_t)a.num_kv_heads * D;
+  const uint32_t region = a.kv_region;
+  // bytes one 16-token slice brings in (K and V) on the TMA path
+  const uint32_t slice_bytes = (uint32_t)(D / 64) * a.HC * 16 * 128 * 2;
+  // Page indices come from a register window of 64 consecutive page-list entries (two 32-lane
+  // halves) whose upper half is loaded 32 pages before it is needed, so the copies of a stage
+  // never wait on a global load.  Usable when one stage spans at most 33 pages.
+  const bool windowed = (Ts - 1) / ps + 2 <= 32;
 
-  int64_t sumL = 0;
-  for (int i = lane; i < a.batch; i += 32) sumL += max(0, __ldg(a.kv_lens + i));
-  sumL = warp_sum(sumL);
-  const int64_t T = sumL * nhg;
+  int64_t sumS = 0;  // 16-token slices over all requests
+  for (int i = lane; i < a.batch; i += 32) sumS += (max(0, __ldg(a.kv_lens + i)) + 15) / 16;
+  sumS = warp_sum(sumS);
+  const int64_t T = sumS * nhg;
   int64_t share = (T + gridDim.x - 1) / gridDim.x;
-  share = ((share + 15) / 16) * 16;
-  if (share < 16) share = 16;
+  if (share < 1) share = 1;
   const int64_t c0 = (int64_t)blockIdx.x * share;
   const int64_t c1 = min(T, c0 + share);
 
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
+
+  int32_t cur_p0 = 0, cur_p1 = 0;  // page list of the request being streamed
+  int win_b = -1, wbase = 0;
+  int32_t w0 = -1, w1 = -1;
+
+  auto entry = [&](int pidx) -> int32_t {  // page-list entry pidx of the current request; -1 past its end
+    const int64_t s = (int64_t)cur_p0 + pidx;
+    return (pidx >= 0 && s < cur_p1) ? __ldg(a.kv_indices + s) : -1;
+  };
+  auto window_page = [&](int pidx) -> int32_t {  // all lanes must call
+    const int k = pidx - wbase;
+    const int32_t v0 = __shfl_sync(0xffffffffu, w0, k & 31);
+    const int32_t v1 = __shfl_sync(0xffffffffu, w1, k & 31);
+    return k < 32 ? v0 : v1;
+  };
 
   auto next_stage = [&]() {
     if (++stage == NS) {
@@ -119,6 +147,20 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   };
 
   auto emit = [&](int unit, int b, int hg, int tok0, int ntok, int flags) -> bool {
+    if (unit >= 0 && windowed) {
+      const int first_page = tok0 / ps;
+      if (b != win_b || first_page < wbase) {  // new request or restart from its first page
+        win_b = b;
+        wbase = first_page;
+        w0 = entry(wbase + lane);
+        w1 = entry(wbase + 32 + lane);
+      }
+      while (first_page >= wbase + 32) {
+        w0 = w1;
+        wbase += 32;
+        w1 = entry(wbase + 32 + lane);
+      }
+    }
     if (!mbar_wait(&empty[stage], phase ^ 1)) {
       if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
       return false;
@@ -135,50 +177,79 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
       h.pad = 0;
       hdr[stage] = h;
     }
-    uint8_t* kst = stages + (size_t)stage * 2 * Ts * RS;
-    uint8_t* vst = kst + (size_t)Ts * RS;
+    uint8_t* kst = stages + (size_t)stage * 2 * region;
+    uint8_t* vst = kst + region;
     if (unit < 0) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[stage]);
       next_stage();
       return true;
     }
-    const int32_t p0 = __ldg(a.kv_indptr + b), p1 = __ldg(a.kv_indptr + b + 1);
-    // up to 4 rows per lane (stage_tokens <= 128)
-    int64_t src[4];
-    int nvalid = 0;
-    uint32_t bad = 0;
+    if constexpr (TMA) {
+      // lane s < W fetches slice s of the stage: 16 tokens inside one page
+      const int tok = tok0 + 16 * lane;
+      const bool in = lane < W && tok < tok0 + ntok;
+      const int pidx = tok / ps;
+      const int32_t page = windowed ? window_page(pidx) : (in ? entry(pidx) : -1);
+      int row = -1;
+      uint32_t bad = 0;
+      if (in) {
+        if ((int64_t)cur_p0 + pidx >= cur_p1)
+          bad = PKV_DEVERR_LENGTH;
+        else if (page < 0 || page >= a.num_pages)
+          bad = PKV_DEVERR_PAGE_OOB;
+        else
+          row = page * ps + tok % ps;
+      }
+      if (bad) report(a.err_word, bad);
+      const int nload = __popc(__ballot_sync(0xffffffffu, row >= 0));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nload * slice_bytes);
+      __syncwarp();
+      if (row >= 0) {
+        const uint32_t slice_off = (uint32_t)lane * a.HC * 2048;
+        const uint32_t half_stride = (uint32_t)W * a.HC * 2048;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int j = lane + 32 * r;
-      src[r] = -1;
-      if (j < ntok) {
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tma_load_3d(smem_u32(kst) + hf * half_stride + slice_off, &a.tm_k, hf * 64, row, hg * a.HC, &full[stage]);
+          tma_load_3d(smem_u32(vst) + hf * half_stride + slice_off, &a.tm_v, hf * 64, row, hg * a.HC, &full[stage]);
+        }
+      }
+    } else {
+      // up to 4 rows per lane (stage_tokens <= 128), one bulk copy per token row
+      int64_t src[4];
+      int nvalid = 0;
+      uint32_t bad = 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = lane + 32 * r;
         const int pos = tok0 + j;
-        const int64_t pslot = (int64_t)p0 + pos / a.page_size;
-        if (pslot >= p1) {
-          bad |= PKV_DEVERR_LENGTH;
-        } else {
-          const int64_t page = __ldg(a.kv_indices + pslot);
-          if (page < 0 || page >= a.num_pages) {
+        const int pidx = pos / ps;
+        const int32_t page = windowed ? window_page(pidx) : (j < ntok ? entry(pidx) : -1);
+        src[r] = -1;
+        if (j < ntok) {
+          if ((int64_t)cur_p0 + pidx >= cur_p1) {
+            bad |= PKV_DEVERR_LENGTH;
+          } else if (page < 0 || page >= a.num_pages) {
             bad |= PKV_DEVERR_PAGE_OOB;
           } else {
-            src[r] = (page * a.page_size + pos % a.page_size) * row_elems + (int64_t)hg * a.HC * D;
+            src[r] = ((int64_t)page * ps + pos % ps) * row_elems + (int64_t)hg * a.HC * D;
             ++nvalid;
           }
         }
       }
-    }
-    if (bad) report(a.err_word, bad);
-    const int tot = warp_sum(nvalid);
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)tot * RB * 2);
-    __syncwarp();
+      if (bad) report(a.err_word, bad);
+      const int tot = warp_sum(nvalid);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)tot * RB * 2);
+      __syncwarp();
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if (src[r] >= 0) {
-        const int j = lane + 32 * r;
-        bulk_g2s(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage]);
-        bulk_g2s(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage]);
+      for (int r = 0; r < 4; ++r) {
+        if (src[r] >= 0) {
+          const int j = lane + 32 * r;
+          bulk_g2s(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage]);
+          bulk_g2s(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage]);
+        }
       }
     }
     next_stage();
@@ -186,37 +257,45 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   };
 
   if (c0 < c1) {
-    int64_t base = 0;  // stream offset of request b0
+    int64_t base = 0;  // stream offset (in slices) of request b0
     for (int b0 = 0; b0 < a.batch && base < c1 && ok; b0 += 32) {
       const int b = b0 + lane;
-      const int64_t L = (b < a.batch) ? (int64_t)max(0, __ldg(a.kv_lens + b)) : 0;
-      int64_t incl = L;
+      const bool in = b < a.batch;
+      const int64_t L = in ? (int64_t)max(0, __ldg(a.kv_lens + b)) : 0;
+      const int64_t S = (L + 15) / 16;
+      const int32_t ip0 = in ? __ldg(a.kv_indptr + b) : 0;
+      const int32_t ip1 = in ? __ldg(a.kv_indptr + b + 1) : 0;
+      int64_t incl = S;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += t;
       }
-      const int64_t rs = base + nhg * (incl - L);
+      const int64_t rs = base + nhg * (incl - S);
       const int64_t re = base + nhg * incl;
-      uint32_t mask = __ballot_sync(0xffffffffu, b < a.batch && L > 0 && re > c0 && rs < c1);
+      uint32_t mask = __ballot_sync(0xffffffffu, in && S > 0 && re > c0 && rs < c1);
       while (mask && ok) {
         const int src_lane = __ffs(mask) - 1;
         mask &= mask - 1;
         const int bb = b0 + src_lane;
         const int64_t Lb = __shfl_sync(0xffffffffu, L, src_lane);
+        const int64_t Sb = __shfl_sync(0xffffffffu, S, src_lane);
         const int64_t rsb = __shfl_sync(0xffffffffu, rs, src_lane);
+        cur_p0 = __shfl_sync(0xffffffffu, ip0, src_lane);
+        cur_p1 = __shfl_sync(0xffffffffu, ip1, src_lane);
         for (int hg = 0; hg < nhg && ok; ++hg) {
-          const int64_t us = rsb + (int64_t)hg * Lb, ue = us + Lb;
+          const int64_t us = rsb + (int64_t)hg * Sb, ue = us + Sb;
           const int64_t s0 = max(us, c0), s1 = min(ue, c1);
           if (s0 >= s1) continue;
-          const int t0 = (int)(s0 - us), t1 = (int)(s1 - us);
+          const int t0 = (int)(s0 - us) * 16;
+          const int t1 = (int)min((s1 - us) * 16, Lb);
           const int unit = bb * nhg + hg;
           for (int t = t0; t < t1 && ok; t += Ts) {
             int flags = 0;
             if (t == t0) flags |= kSegFirst;
             if (t + Ts >= t1) flags |= kSegLast;
-            if (t0 == 0) flags |= kStartsUnit;
-            if (t1 == (int)Lb) flags |= kEndsUnit;
+            if (s0 == us) flags |= kStartsUnit;
+            if (s1 == ue) flags |= kEndsUnit;
             ok = emit(unit, bb, hg, t, min(Ts, t1 - t), flags);
           }
         }
@@ -230,7 +309,7 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
 // ---------------------------------------------------------------------------------------------
 // Consumers: 16-token slices of one KV head with its G query heads.
 // ---------------------------------------------------------------------------------------------
-template <int D, int NT>
+template <int D, int NT, bool TMA>
 __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* hdr,
                                 uint64_t* full, uint64_t* empty, float* mbuf) {
   constexpr int KS = D / 16;
@@ -241,13 +320,24 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   const int hl = warp % HC;  // KV head within the CTA's group
   const int si = warp / HC;  // slice within a stage
   const int g = lane >> 2, c = lane & 3;
-  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  const int NS = a.num_stages, RS = a.row_stride;
+  const uint32_t region = a.kv_region;
   const int HQU = HC * G;  // query heads per unit
 
-  // per-lane ldmatrix row offsets
+  // per-lane ldmatrix addressing.  Row-copy layout: token rows at stride RS, head hl at hl*D*2.
+  // TMA layout: [half][slice][head][16 rows][128 B] with the 16-byte chunks of row t XOR-ed by t%8.
   const int mi = lane >> 3, ri = lane & 7;
-  const uint32_t k_lane_off = (uint32_t)((si * 16 + ri + ((mi & 1) << 3)) * RS + hl * D * 2 + ((mi >> 1) << 3) * 2);
-  const uint32_t v_lane_off = (uint32_t)((si * 16 + ri + ((mi >> 1) << 3)) * RS + hl * D * 2 + ((mi & 1) << 3) * 2);
+  const int kt = ri + ((mi & 1) << 3);  // token row this lane addresses for K
+  const int vt = ri + ((mi >> 1) << 3);  // ... for V
+  uint32_t k_lane_off, v_lane_off;
+  const uint32_t half_stride = (uint32_t)W * HC * 2048;
+  if (TMA) {
+    k_lane_off = (uint32_t)(si * HC * 2048 + hl * 2048 + kt * 128);
+    v_lane_off = (uint32_t)(si * HC * 2048 + hl * 2048 + vt * 128);
+  } else {
+    k_lane_off = (uint32_t)((si * 16 + kt) * RS + hl * D * 2 + ((mi >> 1) << 3) * 2);
+    v_lane_off = (uint32_t)((si * 16 + vt) * RS + hl * D * 2 + ((mi & 1) << 3) * 2);
+  }
   const uint32_t stages_u32 = smem_u32(stages);
 
   uint32_t qf[NT][KS][2];
@@ -288,9 +378,21 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
     }
 
     const int nv = min(16, h.ntok - si * 16);
+    const uint32_t kb = stages_u32 + (uint32_t)stage * 2 * region;
+    const uint32_t vb = kb + region;
+    if (TMA && nv > 0 && nv < 16) {
+      // a partial slice: the TMA box also brought rows past the request's end (unused slots,
+      // possibly NaN); zero this head's V rows there so that P = 0 times V stays 0
+      uint8_t* vrow = stages + (size_t)stage * 2 * region + region + si * HC * 2048 + hl * 2048;
+      for (int idx = lane; idx < (16 - nv) * 8 * (D / 64); idx += 32) {
+        const int hf = idx / ((16 - nv) * 8);
+        const int rem = idx - hf * (16 - nv) * 8;
+        *reinterpret_cast<uint4*>(vrow + hf * half_stride + (nv + (rem >> 3)) * 128 + (rem & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
     if (nv > 0) {
-      const uint32_t kb = stages_u32 + (uint32_t)stage * 2 * Ts * RS;
-      const uint32_t vb = kb + (uint32_t)Ts * RS;
       float s[NT][4], s2[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -299,7 +401,14 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(kb + k_lane_off + ks * 32, a0, a1, a2, a3);
+        uint32_t addr;
+        if (TMA) {
+          const int cc = 2 * (ks & 3) + (mi >> 1);  // 16-byte chunk within the 128-byte row
+          addr = kb + (ks >> 2) * half_stride + k_lane_off + ((cc ^ (kt & 7)) << 4);
+        } else {
+          addr = kb + k_lane_off + ks * 32;
+        }
+        ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ks & 1)
@@ -344,11 +453,19 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vb + v_lane_off + mt * 32, a0, a1, a2, a3);
+        uint32_t addr;
+        if (TMA) {
+          const int cc = 2 * (mt & 3) + (mi & 1);
+          addr = vb + (mt >> 2) * half_stride + v_lane_off + ((cc ^ (vt & 7)) << 4);
+        } else {
+          addr = vb + v_lane_off + mt * 32;
+        }
+        ldsm_x4_t(addr, a0, a1, a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
       }
     }
+    if (TMA && nv > 0 && nv < 16) fence_proxy_async_smem();  // zeros above, before the next TMA fill
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
 
@@ -448,13 +565,17 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   }
 }
 
-template <int D, int NT>
+template <int D, int NT, bool TMA>
 __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int NS = a.num_stages, Ts = a.stage_tokens, RS = a.row_stride;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int NS = a.num_stages;
   const int NC = a.HC * a.W;
+  if (TMA && (smem_u32(smem) & 1023u)) {  // the swizzled stage layout needs a 1024-byte base
+    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_INTERNAL);
+    return;
+  }
   uint8_t* stages = smem;
-  const size_t stage_region = (size_t)NS * 2 * Ts * RS;
+  const size_t stage_region = (size_t)NS * 2 * a.kv_region;
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + stage_region);
   uint64_t* full = reinterpret_cast<uint64_t*>(hdr + NS);
   uint64_t* empty = full + NS;
@@ -469,67 +590,81 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const __grid_const
       mbar_init(&empty[s], NC);
     }
     fence_mbar_init();
+    if (TMA) {
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+    }
   }
   fence_proxy_async_smem();
   __syncthreads();
 
+  // the merge kernel may be scheduled now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   if (warp == NC) {
-    decode_producer<D>(a, stages, hdr, full, empty);
+    decode_producer<D, TMA>(a, stages, hdr, full, empty);
   } else if (warp < NC) {
-    decode_consumer<D, NT>(a, stages, hdr, full, empty, mbuf);
+    decode_consumer<D, NT, TMA>(a, stages, hdr, full, empty, mbuf);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// Merge of the decode's split partials: one block per unit (request, head group).
+// Merge of the decode's split partials: one warp per (unit, query head).  Launched as a
+// programmatic dependent of the decode kernel, so it is resident before the decode ends and
+// starts as soon as the decode's writes are visible.
 // ---------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int u = blockIdx.x;
   const int b = u / a.nhg, hg = u % a.nhg;
   const int HQU = a.HC * a.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qhl = blockIdx.y * 8 + warp;
+  if (qhl >= HQU) return;
   constexpr int VPL = D / 32;  // values per lane
+  const int64_t qh = (int64_t)hg * HQU + qhl;
   const int L = __ldg(a.kv_lens + b);
   if (L <= 0) {
-    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_LENGTH);
-    for (int qhl = warp; qhl < HQU; qhl += 4) {
-      const int64_t qh = (int64_t)hg * HQU + qhl;
-      __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D;
+    if (blockIdx.y == 0 && threadIdx.x == 0) report(a.err_word, PKV_DEVERR_LENGTH);
+    __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) op[lane * VPL + i] = __float2bfloat16_rn(0.f);
-      if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = -INFINITY;
-    }
+    for (int i = 0; i < VPL; ++i) op[lane * VPL + i] = __float2bfloat16_rn(0.f);
+    if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = -INFINITY;
     return;
   }
   const int first = a.unit_first[u], last = a.unit_last[u];
   if (first == last) return;  // the decode kernel wrote this unit's output directly
   if (first < 0 || last >= a.num_parts || last < first) {
-    if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
     return;
   }
-  for (int qhl = warp; qhl < HQU; qhl += 4) {
-    float mx = -INFINITY;
-    for (int p = first; p <= last; ++p) mx = fmaxf(mx, a.part_lse[(int64_t)p * HQU + qhl]);
-    float acc[VPL];
+  float mx = -INFINITY;
+  for (int p = first + lane; p <= last; p += 32) mx = fmaxf(mx, a.part_lse[(int64_t)p * HQU + qhl]);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
-    float tot = 0.f;
-    for (int p = first; p <= last; ++p) {
-      const float w = __expf(a.part_lse[(int64_t)p * HQU + qhl] - mx);
-      tot += w;
-      const float* pp = a.part_o + ((int64_t)p * HQU + qhl) * D + lane * VPL;
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float acc[VPL];
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) acc[i] += w * pp[i];
+  for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+  float tot = 0.f;
+  for (int p0 = first; p0 <= last; p0 += 32) {
+    const int p = p0 + lane;
+    const float w = p <= last ? __expf(a.part_lse[(int64_t)p * HQU + qhl] - mx) : 0.f;
+    tot += warp_sum(w);
+    const int n = min(32, last - p0 + 1);
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, i);
+      const float* pp = a.part_o + ((int64_t)(p0 + i) * HQU + qhl) * D + lane * VPL;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) acc[v] += wi * pp[v];
     }
-    const float inv = 1.f / tot;
-    const int64_t qh = (int64_t)hg * HQU + qhl;
-    __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D + lane * VPL;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) op[i] = __float2bfloat16_rn(acc[i] * inv);
-    if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = mx + logf(tot);
   }
+  const float inv = 1.f / tot;
+  __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D + lane * VPL;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) op[i] = __float2bfloat16_rn(acc[i] * inv);
+  if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = mx + logf(tot);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -579,6 +714,8 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const float* __restri
 // ---------------------------------------------------------------------------------------------
 struct DecodePlan {
   int HC, nhg, W, G, NT, Ts, RS, NS;
+  bool tma;
+  uint32_t region;
   size_t smem;
   int ncta;
   int64_t nunits, nparts;
@@ -589,7 +726,8 @@ constexpr size_t kSmemBudget = 225 * 1024;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p) {
+bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p, int page_size = 0,
+               int64_t num_pages = 0) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return false;
   if (D != 64 && D != 128) return false;
   p.G = Hq / Hkv;
@@ -604,7 +742,10 @@ bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p) {
   p.Ts = 16 * p.W;
   const int RB = p.HC * D * 2;
   p.RS = RB + (((RB / 16) % 2 == 0) ? 16 : 0);
-  const size_t stage = (size_t)2 * p.Ts * p.RS;
+  // 16-token slices lie inside one page when the page size is a multiple of 16
+  p.tma = page_size > 0 && page_size % 16 == 0 && num_pages * (int64_t)page_size < 0x7fffffffLL;
+  p.region = p.tma ? (uint32_t)(D / 64) * p.W * p.HC * 2048 : (uint32_t)(p.Ts * p.RS);
+  const size_t stage = (size_t)2 * p.region;
   const int mf = 4 * p.NT + (D / 16) * p.NT * 4;
   const size_t mbytes = p.W > 1 ? (size_t)(p.W - 1) * p.HC * mf * 32 * 4 : 0;
   const size_t fixed = mbytes + (size_t)kMaxStages * (sizeof(StageHdr) + 16);
@@ -624,9 +765,9 @@ bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p) {
   return true;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool TMA>
 pkv_status launch_decode(const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
-  auto kern = paged_decode_kernel<D, NT>;
+  auto kern = paged_decode_kernel<D, NT, TMA>;
   static int configured_dev[64] = {0};
   const int dev = pkv_host::current_device();
   if (dev >= 0 && dev < 64 && configured_dev[dev] < (int)p.smem) {
@@ -640,7 +781,17 @@ pkv_status launch_decode(const DecodePlan& p, const DecodeArgs& a, cudaStream_t 
   pkv_status s = pkv_host::launch_status();
   if (s != PKV_OK) return s;
   if (p.nunits > 0) {
-    decode_merge_kernel<D><<<(unsigned)p.nunits, 128, 0, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.nunits, (unsigned)((p.HC * p.G + 7) / 8), 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a) != cudaSuccess) return PKV_ERR_CUDA;
     s = pkv_host::launch_status();
   }
   return s;
@@ -674,7 +825,8 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
   const int ncta = pkv_host::sm_count();
   if (ncta <= 0) return PKV_ERR_CUDA;
   DecodePlan p;
-  if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, D, ncta, p)) return PKV_ERR_UNSUPPORTED;
+  if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, D, ncta, p, pool->page_size, pool->num_pages))
+    return PKV_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < p.ws_bytes) return PKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
 
@@ -707,12 +859,30 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
   a.stage_tokens = p.Ts;
   a.num_stages = p.NS;
   a.num_parts = (int32_t)p.nparts;
+  a.kv_region = p.region;
+  bool tma = p.tma;
+  if (tma) {
+    const uint64_t Hkv = pool->num_kv_heads;
+    const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
+    tma = pkv_host::encode_tmap_3d(&a.tm_k, pool->k, D, rows, Hkv, Hkv * D * 2, (uint64_t)D * 2, 64, 16,
+                                   p.HC) &&
+          pkv_host::encode_tmap_3d(&a.tm_v, pool->v, D, rows, Hkv, Hkv * D * 2, (uint64_t)D * 2, 64, 16,
+                                   p.HC);
+    if (!tma) {  // fall back to row copies with the matching stage layout
+      p.tma = false;
+      if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, D, ncta, p)) return PKV_ERR_UNSUPPORTED;
+      a.num_stages = p.NS;
+      a.kv_region = p.region;
+    }
+  }
 
   cudaStream_t st = (cudaStream_t)stream;
-  if (D == 128) {
-    return p.NT == 1 ? launch_decode<128, 1>(p, a, st) : launch_decode<128, 2>(p, a, st);
+  if (p.tma) {
+    if (D == 128) return p.NT == 1 ? launch_decode<128, 1, true>(p, a, st) : launch_decode<128, 2, true>(p, a, st);
+    return p.NT == 1 ? launch_decode<64, 1, true>(p, a, st) : launch_decode<64, 2, true>(p, a, st);
   }
-  return p.NT == 1 ? launch_decode<64, 1>(p, a, st) : launch_decode<64, 2>(p, a, st);
+  if (D == 128) return p.NT == 1 ? launch_decode<128, 1, false>(p, a, st) : launch_decode<128, 2, false>(p, a, st);
+  return p.NT == 1 ? launch_decode<64, 1, false>(p, a, st) : launch_decode<64, 2, false>(p, a, st);
 }
 
 pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,

@@ -15,14 +15,14 @@
 //    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
 //  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=2x64, K=64) run as tcgen05.mma issued
 //    by one thread, accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.
-//  * Four softmax warps own one row each per thread: they read S from TMEM, apply the causal
-//    mask and the online softmax in fp32 (the running max is only moved when it grows by more
-//    than 2^8, so O is rescaled in TMEM rarely), write P as bf16 into shared memory in the
-//    swizzled K-major layout the PV MMA reads, and finally normalise O and store it.
+//  * Eight softmax warps, two per TMEM lane quadrant: a thread owns one row and one half of the
+//    tile's columns.  It reads the whole S row from TMEM for the row max (no cross-warp exchange),
+//    applies the causal mask and the online softmax in fp32 on its half (the running max only
+//    moves when it grows by more than 2^8, so O is rescaled in TMEM rarely), writes its half of P
+//    as bf16 into shared memory in the swizzled K-major layout the PV MMA reads, and finally
+//    normalises its half of the O row and stores it.
 //  * Two CTAs fit on an SM (112 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
-#include <cudaTypedefs.h>
-
 #include "tc05.cuh"
 
 namespace {
@@ -32,7 +32,8 @@ using namespace pkv;
 constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
 constexpr int kBN = 64;   // KV positions per tile
 constexpr int kHD = 128;  // head_dim
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 256); S buffers at [0,64) and [64,128)
 
@@ -83,55 +84,66 @@ struct Work {
   int h, b, qo0, E, t0, P, L, kv_end, n_tiles;
 };
 
-// TMA row coordinate of box i of KV tile j, or -1 when the box is not loaded.
-__device__ __forceinline__ int kv_box_row(const ExtendArgs& a, const Work& w, int p0, int np, int j,
-                                          int i, int R, bool report_errors) {
-  const int pos0 = j * kBN + i * R;
-  if (pos0 >= w.kv_end) return -1;
-  const int pidx = pos0 >> a.log2_ps;
-  if (pidx >= np) {
-    if (report_errors) report(a.err_word, PKV_DEVERR_LENGTH);
-    return -1;
-  }
-  const int64_t page = __ldg(a.kv_indices + p0 + pidx);
-  if (page < 0 || page >= a.num_pages) {
-    if (report_errors) report(a.err_word, PKV_DEVERR_PAGE_OOB);
-    return -1;
-  }
-  return (int)(page * a.page_size + (pos0 & (a.page_size - 1)));
-}
-
+// Producer warp: Q once, then K and V tiles page by page.  Lane i issues box i of a tile; the
+// page indices come from a register window of 64 page-list entries whose upper half is loaded
+// 32 pages before it is needed, so no TMA waits on a dependent global load.
 __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w) {
+  const int lane = threadIdx.x & 31;
   const int G = a.group;
-  mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-  tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.qo0 + w.t0, &bars->q_full);
-  tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.qo0 + w.t0, &bars->q_full);
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+    tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.qo0 + w.t0, &bars->q_full);
+    tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.qo0 + w.t0, &bars->q_full);
+  }
   const int p0 = __ldg(a.kv_indptr + w.b);
   const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
-  const int R = min(a.page_size, kBN);
-  const int nbox = kBN / R;
+  const int R = min(a.page_size, kBN);  // rows per box (a power of two, >= 8)
+  const int nbox = kBN / R;             // boxes per tile (<= 8)
+  auto entry = [&](int pidx) -> int32_t {
+    return (pidx >= 0 && pidx < np) ? __ldg(a.kv_indices + p0 + pidx) : -1;
+  };
+  int wbase = 0;
+  int32_t w0 = entry(lane), w1 = entry(32 + lane);
   for (int j = 0; j < w.n_tiles; ++j) {
     const int st = j & 1;
     const uint32_t ph = (j >> 1) & 1;
+    // box `lane` of tile j: positions [pos0, pos0 + R)
+    const int pos0 = j * kBN + lane * R;
+    const int pidx = pos0 >> a.log2_ps;
+    while ((j * kBN >> a.log2_ps) >= wbase + 32) {
+      w0 = w1;
+      wbase += 32;
+      w1 = entry(wbase + 32 + lane);
+    }
+    const int k = pidx - wbase;  // < 64: a tile spans at most 8 pages past the window base
+    const int32_t v0 = __shfl_sync(0xffffffffu, w0, k & 31);
+    const int32_t v1 = __shfl_sync(0xffffffffu, w1, k & 31);
+    const int32_t page = k < 32 ? v0 : v1;
+    int row = -1;
+    if (lane < nbox && pos0 < w.kv_end) {
+      if (pidx >= np)
+        report(a.err_word, PKV_DEVERR_LENGTH);
+      else if (page < 0 || page >= a.num_pages)
+        report(a.err_word, PKV_DEVERR_PAGE_OOB);
+      else
+        row = (int)((int64_t)page * a.page_size + (pos0 & (a.page_size - 1)));
+    }
+    const uint32_t nload = __popc(__ballot_sync(0xffffffffu, row >= 0));
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
       uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
       uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
       const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
-      if (!mbar_wait(empty, ph ^ 1)) {
-        report(a.err_word, PKV_DEVERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1))) {
+        if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
         return false;
       }
-      int nload = 0;
-      for (int i = 0; i < nbox; ++i) nload += kv_box_row(a, w, p0, np, j, i, R, false) >= 0;
-      mbar_arrive_expect_tx(full, (uint32_t)nload * R * 128 * 2);
-      const uint32_t base = sb + (kv ? kOffV : kOffK) + st * kKVStage;
-      for (int i = 0; i < nbox; ++i) {
-        const int z = kv_box_row(a, w, p0, np, j, i, R, kv == 0);
-        if (z < 0) continue;
-        const uint32_t dst = base + i * R * 128;
-        tma_load_3d(dst, tm, 0, w.h, z, full);
-        tma_load_3d(dst + kKVHalf, tm, 64, w.h, z, full);
+      if (lane == 0) mbar_arrive_expect_tx(full, nload * R * 128 * 2);
+      __syncwarp();
+      if (row >= 0) {
+        const uint32_t dst = sb + (kv ? kOffV : kOffK) + st * kKVStage + lane * R * 128;
+        tma_load_3d(dst, tm, 0, w.h, row, full);
+        tma_load_3d(dst + kKVHalf, tm, 64, w.h, row, full);
       }
     }
   }
@@ -180,11 +192,22 @@ __device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_
   return issue_pv(w.n_tiles - 1);
 }
 
+template <int N>
+__device__ __forceinline__ float tree_max(float (&v)[N]) {
+#pragma unroll
+  for (int w = N / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) v[i] = fmaxf(v[i], v[i + w]);
+  return v[0];
+}
+
 __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, uint32_t tmem,
                                const Work& w) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp & 3;        // TMEM lane quadrant this warp may access
-  const int r = wq * 32 + lane;   // tile row == TMEM lane
+  const int wq = warp & 3;            // TMEM lane quadrant this warp may access
+  const int hsel = (warp - 2) >> 2;   // which half of the tile's columns this warp owns
+  const int r = wq * 32 + lane;       // tile row == TMEM lane
+  const int tid = (warp - 2) * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
   const int G = a.group;
   const int tok = w.t0 + (r >> a.log2_group);
@@ -192,7 +215,12 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   const bool valid = tok < w.E;
   const int limit = min(w.P + tok, w.L - 1);  // last visible KV position of this row
   const int min_limit = w.P + w.t0;            // smallest limit over the tile's rows
-  float m_used = -INFINITY, l = 0.f;
+  // scores are scaled inside one FFMA, x = s * scale - m * scale; with a non-positive scale the
+  // max of s is not the max of the scaled scores, so scale first
+  const bool pos_scale = a.scale_log2 > 0.f;
+  const float sc = pos_scale ? a.scale_log2 : 1.f;
+  float m_used = -INFINITY;  // running max of the scaled (log2) scores
+  float l = 0.f;             // this half's running sum
   bool ok = true;
 
   for (int j = 0; j < w.n_tiles; ++j) {
@@ -200,50 +228,55 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[st], (j >> 1) & 1));
     if (!ok) break;
     tc_fence_after();
-    float s[64];
-    {
-      float lo[32], hi[32];
-      tmem_ld32(taddr + st * 64, lo);
-      tmem_ld32(taddr + st * 64 + 32, hi);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = lo[c];
-        s[32 + c] = hi[c];
-      }
-    }
+    float so[32], sm[32];  // the other half's and this half's scores of the row
+    tmem_ld32(taddr + st * 64 + (hsel ^ 1) * 32, so);
+    tmem_ld32(taddr + st * 64 + hsel * 32, sm);
+    tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->s_free[st]);
 
     const int pos0 = j * kBN;
-    float mx = -INFINITY;
-    if (pos0 + kBN - 1 <= min_limit) {
+    if (!pos_scale) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] *= a.scale_log2;
-        mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < 32; ++c) {
+        so[c] *= a.scale_log2;
+        sm[c] *= a.scale_log2;
       }
-    } else {
+    }
+    if (pos0 + kBN - 1 > min_limit) {  // the causal diagonal crosses this tile
+      const int pm = pos0 + hsel * 32, po = pos0 + (hsel ^ 1) * 32;
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = (pos0 + c <= limit) ? s[c] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < 32; ++c) {
+        sm[c] = (pm + c <= limit) ? sm[c] : -INFINITY;
+        so[c] = (po + c <= limit) ? so[c] : -INFINITY;
       }
+    }
+    float mx;
+    {
+      float t[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) t[c] = fmaxf(so[c], sm[c]);
+      mx = tree_max(t) * sc;
     }
     const float m_new = fmaxf(m_used, mx);
     const bool resc = m_new > m_used + 8.f;  // always true on the first tile (m_used = -inf)
     const float m_ref = resc ? m_new : m_used;
     const float corr = resc ? ex2(m_used - m_ref) : 1.f;
-    uint32_t pk[kBN / 2];
-    float sum = 0.f;
+    uint32_t pk[16];
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-    for (int c = 0; c < kBN / 2; ++c) {
-      const float p0 = ex2(s[2 * c] - m_ref), p1 = ex2(s[2 * c + 1] - m_ref);
-      sum += p0 + p1;
+    for (int c = 0; c < 16; c += 2) {
+      const float p0 = ex2(fmaf(sm[2 * c], sc, -m_ref)), p1 = ex2(fmaf(sm[2 * c + 1], sc, -m_ref));
+      const float p2 = ex2(fmaf(sm[2 * c + 2], sc, -m_ref)), p3 = ex2(fmaf(sm[2 * c + 3], sc, -m_ref));
+      acc0 += p0;
+      acc1 += p1;
+      acc2 += p2;
+      acc3 += p3;
       pk[c] = pack_bf16x2(p0, p1);
+      pk[c + 1] = pack_bf16x2(p2, p3);
     }
-    l = l * corr + sum;
+    l = l * corr + ((acc0 + acc1) + (acc2 + acc3));
     m_used = m_ref;
 
     if (j > 0) {
@@ -252,13 +285,14 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
       tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-        for (int ch = 0; ch < kHD / 32; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
           float o[32];
-          tmem_ld32(taddr + kColO + ch * 32, o);
+          const uint32_t oc = taddr + kColO + hsel * 64 + ch * 32;
+          tmem_ld32(oc, o);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tmem_st32(taddr + kColO + ch * 32, o);
+          tmem_st32(oc, o);
         }
         tmem_wait_st();
       }
@@ -271,7 +305,7 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
       const int r0 = w.kv_end - pos0;
       const int nchunks = (kBN - r0) * 8 * 2;  // rows x 16-byte chunks x halves
       uint8_t* vb = smem + kOffV + st * kKVStage;
-      for (int idx = r; idx < nchunks; idx += kBM) {
+      for (int idx = tid; idx < nchunks; idx += kSoftmaxWarps * 32) {
         const int half = idx & 1, rc = idx >> 1;
         const int row = r0 + (rc >> 3), ch = rc & 7;
         *reinterpret_cast<uint4*>(vb + half * kKVHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -279,9 +313,11 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     }
     uint8_t* prow = smem + kOffP + r * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+    for (int c = 0; c < 4; ++c) {
+      const int chunk = hsel * 4 + c;
+      *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) =
           make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
@@ -294,13 +330,18 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     return;
   }
   tc_fence_after();
-  const float inv = 1.f / l;
+  // the two halves' sums meet in the (now idle) P buffer
+  float* lbuf = reinterpret_cast<float*>(smem + kOffP);
+  lbuf[hsel * kBM + r] = l;
+  named_bar_sync(1, kSoftmaxWarps * 32);
+  const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
+  const float inv = 1.f / l_tot;
   const int64_t row = (int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g;
-  uint4* orow = reinterpret_cast<uint4*>(a.out + row * kHD);
+  uint4* orow = reinterpret_cast<uint4*>(a.out + row * kHD + hsel * 64);
 #pragma unroll 1
-  for (int ch = 0; ch < kHD / 32; ++ch) {
+  for (int ch = 0; ch < 2; ++ch) {
     float o[32];
-    tmem_ld32(taddr + kColO + ch * 32, o);
+    tmem_ld32(taddr + kColO + hsel * 64 + ch * 32, o);
     tmem_wait_ld();
     if (valid) {
 #pragma unroll
@@ -311,13 +352,14 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
                                       pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
     }
   }
-  if (valid && a.lse) a.lse[row] = (m_used + log2f(l)) * kLn2;
+  if (valid && hsel == 0 && a.lse) a.lse[row] = (m_used + log2f(l_tot)) * kLn2;
 }
 
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Work w;
-  w.t0 = blockIdx.x * a.tokens_per_tile;
+  // later tiles of a request attend over more positions: launch them first
+  w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
   w.h = blockIdx.y;
   w.b = blockIdx.z;
   w.qo0 = __ldg(a.qo_indptr + w.b);
@@ -343,9 +385,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 4);
+      mbar_init(&bars->s_free[s], kSoftmaxWarps);
     }
-    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_full, kSoftmaxWarps);
     mbar_init(&bars->pv_done, 1);
     fence_mbar_init();
     prefetch_tmap(&a.tm_q);
@@ -362,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0 && !extend_producer(a, sb, bars, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    extend_producer(a, sb, bars, w);
   } else if (warp == 1) {
     if (lane == 0 && !extend_mma(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
     __syncwarp();
@@ -380,32 +422,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
 // ---------------------------------------------------------------------------------------------
 // Host
 // ---------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-               uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {s1, s2};
-  cuuint32_t box[3] = {b0, b1, b2};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int log2_exact(int x) {
   if (x <= 0 || (x & (x - 1))) return -1;
   int l = 0;
@@ -456,9 +472,9 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
   const uint64_t Hq = num_q_heads, Hkv = pool->num_kv_heads;
   const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
   const uint32_t R = pool->page_size < kBN ? pool->page_size : kBN;
-  if (!encode_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_tokens, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
-      !encode_3d(&a.tm_k, pool->k, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R) ||
-      !encode_3d(&a.tm_v, pool->v, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R))
+  if (!pkv_host::encode_tmap_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_tokens, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
+      !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R) ||
+      !pkv_host::encode_tmap_3d(&a.tm_v, pool->v, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R))
     return PKV_ERR_CUDA;
   a.qo_indptr = qo_indptr;
   a.kv_indptr = kv_indptr;

@@ -116,3 +116,10 @@ PKV_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: 
 PKV_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace pkv
+
+namespace pkv_host {
+// 3-D bf16 tensor map with 128-byte swizzle: dims {d0 (contiguous), d1, d2}, byte strides of
+// d1 and d2, box {b0, b1, b2}.  False if the driver rejects it.  Defined in abi.cu.
+bool encode_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
+}  // namespace pkv_host
