@@ -82,7 +82,7 @@ def workload_counts(b):
     for r in range(len(lens)):
         pos = np.arange(lens[r])
         slots.append(indices[indptr[r] + pos // ps] * ps + pos % ps)
-    uniq = np.unique(np.concatenate(slots)).size if slots else 0
+    uniq = np.unique(np.concatenate(slots)).size if len(slots) else 0
     logical = int(lens.sum())
     qo_bytes = len(lens) * Hq * D * 2 * 2 + len(lens) * Hq * 4  # q in, out + lse
     meta = (indptr.size + indices.size + lens.size) * 4
@@ -263,15 +263,20 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)  # let the sampler take its first reading
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     with torch.cuda.stream(st):
         start.record(st)
         for k in range(K):
+            if flush is not None:
+                flush.zero_()
             step(evs[k])
         stop.record(st)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     elapsed_ms = start.elapsed_time(stop)
+    if flush is not None:  # exclude the flushes: the step is the span of its own operations
+        elapsed_ms = sum(e[0].elapsed_time(e[3]) for e in evs)
     t_app = [e[0].elapsed_time(e[1]) for e in evs]
     t_dec = [e[1].elapsed_time(e[2]) for e in evs]
     t_ext = [e[2].elapsed_time(e[3]) for e in evs]
@@ -323,13 +328,38 @@ def run_ours(args, ws, rank, local):
     ms_step = elapsed_ms / K
     tokens = counts["attn_tokens"]
     value = tokens * K * ws / (elapsed_ms / 1e3)
-    dec_ms = statistics.mean(t_dec)
-    ext_ms = statistics.mean(t_ext)
-    app_ms = statistics.mean(t_app)
-    dec_gbs = counts["decode_bytes"] / (dec_ms / 1e3) / 1e9
-    ext_tflops = counts["extend_flops"] / (ext_ms / 1e3) / 1e12
-    app_gbs = counts["append_bytes"] / (app_ms / 1e3) / 1e9
-    traffic = _traffic_record()
+    dec_ms = statistics.mean(t_dec) if do_dec else None
+    ext_ms = statistics.mean(t_ext) if do_ext else None
+    app_ms = statistics.mean(t_app) if (do_app and b.num_new_tokens) else None
+    kernels = {}
+    if dec_ms:
+        dec_gbs = counts["decode_bytes"] / (dec_ms / 1e3) / 1e9
+        kernels["decode"] = {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
+                             "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
+                             "gbs_logical": round(counts["decode_bytes_logical"] / (dec_ms / 1e3) / 1e9, 1)}
+    # the extend runs alone in its step on the radix-extend workload (burst peak), inside a long
+    # step otherwise (sustained peak)
+    ext_peak = peaks["bf16_tflops"] if not do_dec else peaks["bf16_tflops_sustained"]
+    if ext_ms:
+        ext_tflops = counts["extend_flops"] / (ext_ms / 1e3) / 1e12
+        kernels["extend"] = {"ms": round(ext_ms, 4), "tflops": round(ext_tflops, 1),
+                             "frac_bf16": round(ext_tflops / ext_peak, 4), "peak_tflops": ext_peak,
+                             "flops": counts["extend_flops"]}
+    if app_ms:
+        kernels["kv_append"] = {"ms": round(app_ms, 4),
+                                "gbs": round(counts["append_bytes"] / (app_ms / 1e3) / 1e9, 1)}
+    traffic = _traffic_record() if args.workload == "mixed" else None
+    if dec_ms:
+        roofline = {"kernel": "paged_decode (decode + split merge)", "bound": "hbm",
+                    "achieved": kernels["decode"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": kernels["decode"]["frac_hbm"], "traffic": traffic,
+                    "algorithmic_bytes": counts["decode_bytes"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
+    else:
+        roofline = {"kernel": "paged_extend", "bound": "tensor", "achieved": kernels["extend"]["tflops"],
+                    "peak": ext_peak, "unit": "TFLOP/s", "frac": kernels["extend"]["frac_bf16"],
+                    "traffic": None, "algorithmic_flops": counts["extend_flops"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peaks["source"] == "measured" else "of fallback"}
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -344,38 +374,22 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v, seeded lengths and page permutation)",
         "config": {
-            "workload": "mixed continuous-batching step: kv_append 2304 tokens + paged decode of 256 "
-                        "requests (KV U[512,4096], 64 share a 2048-token prefix) + ragged extend of 4x512 "
-                        "chunked-prefill tokens (prefixes 0/512/1024/1536); Qwen3-8B attention 32q/8kv "
-                        "heads, head_dim 128, page 16",
+            "workload": (b.name if args.workload != "mixed" else
+                         "mixed continuous-batching step: kv_append 2304 tokens + paged decode of 256 "
+                         "requests (KV U[512,4096], 64 share a 2048-token prefix) + ragged extend of 4x512 "
+                         "chunked-prefill tokens (prefixes 0/512/1024/1536); Qwen3-8B attention 32q/8kv "
+                         "heads, head_dim 128, page 16"),
             "decode_requests": b.num_decode, "extend_requests": b.num_extend,
             "new_tokens": b.num_new_tokens, "page_size": b.page_size, "num_pages": b.num_pages,
-            "l2": "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9),
+            "l2": ("L2 flushed (256 MB written) before every step" if args.flush_l2 else
+                   "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9)),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
-        "roofline": {
-            "kernel": "paged_decode (decode + split merge)",
-            "bound": "hbm",
-            "achieved": round(dec_gbs, 1),
-            "peak": peaks["hbm_gbs"],
-            "unit": "GB/s",
-            "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
-            "traffic": traffic,
-            "algorithmic_bytes": counts["decode_bytes"],
-            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "fallback",
-        },
-        "kernels": {
-            "decode": {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
-                       "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
-                       "gbs_logical": round(counts["decode_bytes_logical"] / (dec_ms / 1e3) / 1e9, 1)},
-            "extend": {"ms": round(ext_ms, 4), "tflops": round(ext_tflops, 1),
-                       "frac_bf16": round(ext_tflops / peaks["bf16_tflops_sustained"], 4),
-                       "peak_tflops": peaks["bf16_tflops_sustained"], "flops": counts["extend_flops"]},
-            "kv_append": {"ms": round(app_ms, 4), "gbs": round(app_gbs, 1)},
-        },
+        "roofline": roofline,
+        "kernels": kernels,
         "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": (int(do_app) + 2 * int(do_dec) + int(do_ext)) * K,
+        "gpu_launches": (int(bool(app_ms)) + 2 * int(do_dec) + int(do_ext)) * K,
         "clocks": clk,
     }
     return line
@@ -463,12 +477,15 @@ def run_reference(args, ws, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+WORKLOADS = {"mixed": 5, "tiny": 1, "batched-decode": 2, "radix-extend": 3, "long-decode": 4}
+
+
 def load_workload(name):
-    """The mixed step (default), or a few-hundred-MB case for profiler captures."""
-    if name == "mixed":
+    """The mixed step (default), the other four workloads, or a few-hundred-MB profiler case."""
+    if name in WORKLOADS:
         from workloads import make_config
 
-        return make_config(WORKLOAD_IDX)
+        return make_config(WORKLOADS[name])
     if name == "profile":
         from workloads import random_small_batch
 
@@ -480,7 +497,10 @@ def load_workload(name):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="mixed", choices=["mixed", "profile"])
+    ap.add_argument("--workload", default="mixed", choices=sorted(WORKLOADS) + ["profile"])
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="zero a 256 MB buffer before every timed step (for workloads that fit in L2); "
+                         "the step time is then the sum of the per-operation event times")
     ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--gpus", type=int, default=1)

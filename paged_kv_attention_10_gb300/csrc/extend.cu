@@ -15,13 +15,14 @@
 //    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
 //  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=2x64, K=64) run as tcgen05.mma issued
 //    by one thread, accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.
+//    P is written back as bf16 pairs over the S columns it came from and the PV MMA reads it from
+//    TMEM, so P never passes through shared memory.
 //  * Eight softmax warps, two per TMEM lane quadrant: a thread owns one row and one half of the
-//    tile's columns.  It reads the whole S row from TMEM for the row max (no cross-warp exchange),
-//    applies the causal mask and the online softmax in fp32 on its half (the running max only
-//    moves when it grows by more than 2^8, so O is rescaled in TMEM rarely), writes its half of P
-//    as bf16 into shared memory in the swizzled K-major layout the PV MMA reads, and finally
-//    normalises its half of the O row and stores it.
-//  * Two CTAs fit on an SM (112 KB of shared memory and 256 TMEM columns each), so one CTA's
+//    tile's columns.  The two halves of a row exchange partial maxima through shared memory, apply
+//    the causal mask and the online softmax in fp32 (the running max only moves when it grows by
+//    more than 2^8, so O is rescaled in TMEM rarely), and finally normalise their halves of the O
+//    row and store them.
+//  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include "tc05.cuh"
 
@@ -44,9 +45,9 @@ constexpr uint32_t kKVStage = 2 * kKVHalf;   // 16 KB
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
-constexpr uint32_t kOffP = kOffV + 2 * kKVStage;
-constexpr uint32_t kPBytes = kBM * kBN * 2;  // 16 KB
-constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kOffX = kOffV + 2 * kKVStage;  // row-max exchange [tile parity][half][row]
+constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [half][row]
+constexpr uint32_t kOffBar = kOffL + 2 * kBM * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
 
 struct Bars {
@@ -162,15 +163,17 @@ __device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_
     const uint32_t vb = sb + kOffV + st * kKVStage;
 #pragma unroll
     for (int ks = 0; ks < kBN / 16; ++ks) {
-      const uint64_t adesc = smem_desc_sw128(sb + kOffP + ks * 32, 16, 1024);
+      // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs
+      const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint64_t bdesc = smem_desc_sw128(vb + half * kKVHalf + ks * 2048, 1024, 1024);
-        umma_ss(tmem + kColO + half * 64, adesc, bdesc, idesc_pv, t > 0 || ks > 0);
+        umma_ts(tmem + kColO + half * 64, pa, bdesc, idesc_pv, t > 0 || ks > 0);
       }
     }
     umma_commit(&bars->pv_done);
     umma_commit(&bars->v_empty[st]);
+    umma_commit(&bars->s_free[st]);  // P (in the S buffer) has been consumed
     return true;
   };
   for (int j = 0; j < w.n_tiles; ++j) {
@@ -201,6 +204,16 @@ __device__ __forceinline__ float tree_max(float (&v)[N]) {
   return v[0];
 }
 
+// barrier shared by the two softmax warps of TMEM lane quadrant wq (ids 1..4)
+__device__ __forceinline__ void pair_bar(int wq) {
+  switch (wq) {
+    case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+  }
+}
+
 __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, uint32_t tmem,
                                const Work& w) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -219,6 +232,7 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   // max of s is not the max of the scaled scores, so scale first
   const bool pos_scale = a.scale_log2 > 0.f;
   const float sc = pos_scale ? a.scale_log2 : 1.f;
+  float* xbuf = reinterpret_cast<float*>(smem + kOffX);
   float m_used = -INFINITY;  // running max of the scaled (log2) scores
   float l = 0.f;             // this half's running sum
   bool ok = true;
@@ -228,37 +242,31 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[st], (j >> 1) & 1));
     if (!ok) break;
     tc_fence_after();
-    float so[32], sm[32];  // the other half's and this half's scores of the row
-    tmem_ld32(taddr + st * 64 + (hsel ^ 1) * 32, so);
+    float sm[32];  // this half's scores of the row
     tmem_ld32(taddr + st * 64 + hsel * 32, sm);
     tmem_wait_ld();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->s_free[st]);
 
     const int pos0 = j * kBN;
     if (!pos_scale) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        so[c] *= a.scale_log2;
-        sm[c] *= a.scale_log2;
-      }
+      for (int c = 0; c < 32; ++c) sm[c] *= a.scale_log2;
     }
     if (pos0 + kBN - 1 > min_limit) {  // the causal diagonal crosses this tile
-      const int pm = pos0 + hsel * 32, po = pos0 + (hsel ^ 1) * 32;
+      const int pm = pos0 + hsel * 32;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        sm[c] = (pm + c <= limit) ? sm[c] : -INFINITY;
-        so[c] = (po + c <= limit) ? so[c] : -INFINITY;
-      }
+      for (int c = 0; c < 32; ++c) sm[c] = (pm + c <= limit) ? sm[c] : -INFINITY;
     }
-    float mx;
+    float mine;
     {
       float t[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) t[c] = fmaxf(so[c], sm[c]);
-      mx = tree_max(t) * sc;
+      for (int c = 0; c < 32; ++c) t[c] = sm[c];
+      mine = tree_max(t);
     }
+    // the row max over both halves: exchange partial maxima with the partner warp
+    xbuf[((j & 1) * 2 + hsel) * kBM + r] = mine;
+    pair_bar(wq);
+    const float mx = fmaxf(mine, xbuf[((j & 1) * 2 + (hsel ^ 1)) * kBM + r]) * sc;
     const float m_new = fmaxf(m_used, mx);
     const bool resc = m_new > m_used + 8.f;  // always true on the first tile (m_used = -inf)
     const float m_ref = resc ? m_new : m_used;
@@ -278,8 +286,12 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     }
     l = l * corr + ((acc0 + acc1) + (acc2 + acc3));
     m_used = m_ref;
+    // P (bf16 pairs) over this half's own S columns, which only this warp reads
+    tmem_st16(taddr + st * 64 + hsel * 32, pk);
 
     if (j > 0) {
+      // PV of the previous tile must be done before O is rescaled (and waiting on every phase
+      // keeps this barrier's parity in step)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (j - 1) & 1));
       if (!ok) break;
       tc_fence_after();
@@ -294,9 +306,9 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
           for (int i = 0; i < 32; ++i) o[i] *= corr;
           tmem_st32(oc, o);
         }
-        tmem_wait_st();
       }
     }
+    tmem_wait_st();
     if (j == w.n_tiles - 1 && w.kv_end < pos0 + kBN) {
       // V rows past the last needed position hold stale or unused-slot data; zero them so that
       // P = 0 times V stays 0 in the PV MMA.
@@ -310,15 +322,8 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
         const int row = r0 + (rc >> 3), ch = rc & 7;
         *reinterpret_cast<uint4*>(vb + half * kKVHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
+      fence_proxy_async_smem();
     }
-    uint8_t* prow = smem + kOffP + r * 128;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int chunk = hsel * 4 + c;
-      *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->p_full);
@@ -330,10 +335,10 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     return;
   }
   tc_fence_after();
-  // the two halves' sums meet in the (now idle) P buffer
-  float* lbuf = reinterpret_cast<float*>(smem + kOffP);
+  // the two halves' sums
+  float* lbuf = reinterpret_cast<float*>(smem + kOffL);
   lbuf[hsel * kBM + r] = l;
-  named_bar_sync(1, kSoftmaxWarps * 32);
+  pair_bar(wq);
   const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
   const float inv = 1.f / l_tot;
   const int64_t row = (int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g;
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], kSoftmaxWarps);
+      mbar_init(&bars->s_free[s], 1);
     }
     mbar_init(&bars->p_full, kSoftmaxWarps);
     mbar_init(&bars->pv_done, 1);
