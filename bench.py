@@ -399,7 +399,12 @@ def run_ours(args, ws, rank, local):
 # CPU oracle (reported baseline and reference arm)
 # ---------------------------------------------------------------------------------------------
 def _oracle_sample_runner(b, kp, vp):
-    """A bounded slice of the workload for the oracle: (callable(k), tokens per call)."""
+    """A bounded slice of the workload for the oracle: callable(k) -> attention tokens done.
+
+    Slice k is decode request k (all heads) and up to 8 consecutive query rows of extend chunk k,
+    for whichever of the two the workload has."""
+    import torch as _t
+
     import oracle
 
     B = b.num_decode
@@ -407,21 +412,23 @@ def _oracle_sample_runner(b, kp, vp):
     rows_per_call = 8
 
     def run(k):
-        r = k % B
-        oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
-                            b.page_size, b.sm_scale, requests=[r])
-        e = k % b.num_extend
-        E = qo[e + 1] - qo[e]
-        i0 = (k * rows_per_call) % E
-        # rows_per_call extend queries of chunk e (a contiguous run inside the chunk)
-        sub_qo = [0, min(rows_per_call, E - i0)]
-        import torch as _t
-        q_rows = b.ext_q[qo[e] + i0: qo[e] + i0 + sub_qo[1]]
-        oracle.paged_extend(q_rows, kp, vp, _t.tensor(sub_qo, dtype=_t.int32),
-                            b.ext_kv_indptr[e:e + 2] - b.ext_kv_indptr[e], b.ext_kv_indices[
-                                int(b.ext_kv_indptr[e]):int(b.ext_kv_indptr[e + 1])],
-                            (b.ext_prefix_lens[e:e + 1] + i0).to(_t.int32), b.page_size, b.sm_scale)
-        return 1 + sub_qo[1]
+        done = 0
+        if B:
+            oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
+                                b.page_size, b.sm_scale, requests=[k % B])
+            done += 1
+        if b.num_extend:
+            e = k % b.num_extend
+            E = qo[e + 1] - qo[e]
+            i0 = (k * rows_per_call) % E
+            n = min(rows_per_call, E - i0)
+            q_rows = b.ext_q[qo[e] + i0: qo[e] + i0 + n]
+            lo, hi = int(b.ext_kv_indptr[e]), int(b.ext_kv_indptr[e + 1])
+            oracle.paged_extend(q_rows, kp, vp, _t.tensor([0, n], dtype=_t.int32),
+                                _t.tensor([0, hi - lo], dtype=_t.int32), b.ext_kv_indices[lo:hi],
+                                (b.ext_prefix_lens[e:e + 1] + i0).to(_t.int32), b.page_size, b.sm_scale)
+            done += n
+        return done
 
     return run
 
@@ -439,8 +446,8 @@ def cpu_baseline(b, seconds=12.0):
     el = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
     return {"value": round(toks / el, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{k} slices of the mixed step, each 1 decode request (all 32 heads) + up to 8 "
-                      f"extend query rows of one chunk; {toks} attention tokens in {el:.1f} s; fp64 NumPy, "
+            "sample": f"{k} slices of the workload, each 1 decode request (all heads) and/or up to 8 "
+                      f"extend query rows of one request; {toks} attention tokens in {el:.1f} s; fp64 NumPy, "
                       f"BLAS may use all {cores} affinity cores"}
 
 

@@ -33,7 +33,7 @@ using namespace pkv;
 constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
 constexpr int kBN = 64;   // KV positions per tile
 constexpr int kHD = 128;  // head_dim
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int kThreads = 352;  // warp 0 Q/K loads, warp 1 MMA, warps 2..9 softmax, warp 10 V loads
 constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 256); S buffers at [0,64) and [64,128)
@@ -88,10 +88,12 @@ struct Work {
 // Producer warp: Q once, then K and V tiles page by page.  Lane i issues box i of a tile; the
 // page indices come from a register window of 64 page-list entries whose upper half is loaded
 // 32 pages before it is needed, so no TMA waits on a dependent global load.
-__device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w) {
+// kv = 0: the K warp (also loads Q); kv = 1: the V warp.  Separate warps keep the K stream
+// ahead of the QK MMAs even while the V stream waits for its stage to be freed by PV.
+__device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
   const int lane = threadIdx.x & 31;
   const int G = a.group;
-  if (lane == 0) {
+  if (kv == 0 && lane == 0) {
     mbar_arrive_expect_tx(&bars->q_full, kQBytes);
     tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.qo0 + w.t0, &bars->q_full);
     tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.qo0 + w.t0, &bars->q_full);
@@ -130,8 +132,7 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
         row = (int)((int64_t)page * a.page_size + (pos0 & (a.page_size - 1)));
     }
     const uint32_t nload = __popc(__ballot_sync(0xffffffffu, row >= 0));
-#pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
+    {
       uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
       uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
       const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    extend_producer(a, sb, bars, w);
+  if (warp == 0 || warp == 10) {
+    extend_producer(a, sb, bars, w, warp == 0 ? 0 : 1);
   } else if (warp == 1) {
     if (lane == 0 && !extend_mma(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
     __syncwarp();
