@@ -53,8 +53,8 @@ constexpr uint32_t kSmemBytes = kOffBar + 256;
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
+  uint64_t s_full[2], s_free[2];  // S buffer b: QK written / its P consumed by PV
+  uint64_t p_full[2];              // P of the tile in S buffer b written by the softmax
   uint32_t tmem_base;
   uint32_t pad;
 };
@@ -152,48 +152,66 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   return true;
 }
 
+// One thread issues all MMAs.  QK of tile jq (into S buffer jq&1) needs the K tile and the S
+// buffer back from the PV two tiles earlier; PV of tile jp needs the softmax's P and the V tile.
+// The two streams are polled with non-blocking tests, so a PV whose P is ready never waits
+// behind a QK whose S buffer is not yet free (and the reverse).
 __device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
   constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
   constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, 64, true);
   if (!mbar_wait(&bars->q_full, 0)) return false;
-  auto issue_pv = [&](int t) -> bool {
-    const int st = t & 1;
-    if (!mbar_wait(&bars->p_full, t & 1)) return false;
-    if (!mbar_wait(&bars->v_full[st], (t >> 1) & 1)) return false;
-    tc_fence_after();
-    const uint32_t vb = sb + kOffV + st * kKVStage;
+  const int n = w.n_tiles;
+  int jq = 0, jp = 0;
+  uint64_t t_last = globaltimer_ns();
+  while (jp < n) {
+    bool progressed = false;
+    if (jq < n && jq < jp + 2) {
+      const int st = jq & 1;
+      const uint32_t ph = (jq >> 1) & 1;
+      if (mbar_test(&bars->k_full[st], ph) && mbar_test(&bars->s_free[st], ph ^ 1)) {
+        tc_fence_after();
+        const uint32_t kb = sb + kOffK + st * kKVStage;
 #pragma unroll
-    for (int ks = 0; ks < kBN / 16; ++ks) {
-      // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs
-      const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint64_t bdesc = smem_desc_sw128(vb + half * kKVHalf + ks * 2048, 1024, 1024);
-        umma_ts(tmem + kColO + half * 64, pa, bdesc, idesc_pv, t > 0 || ks > 0);
+        for (int ks = 0; ks < kHD / 16; ++ks) {
+          const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+          umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
+        }
+        umma_commit(&bars->s_full[st]);
+        umma_commit(&bars->k_empty[st]);
+        ++jq;
+        progressed = true;
       }
     }
-    umma_commit(&bars->pv_done);
-    umma_commit(&bars->v_empty[st]);
-    umma_commit(&bars->s_free[st]);  // P (in the S buffer) has been consumed
-    return true;
-  };
-  for (int j = 0; j < w.n_tiles; ++j) {
-    const int st = j & 1;
-    if (!mbar_wait(&bars->k_full[st], (j >> 1) & 1)) return false;
-    if (!mbar_wait(&bars->s_free[st], ((j >> 1) & 1) ^ 1)) return false;
-    tc_fence_after();
-    const uint32_t kb = sb + kOffK + st * kKVStage;
+    if (jp < jq) {
+      const int st = jp & 1;
+      const uint32_t ph = (jp >> 1) & 1;
+      if (mbar_test(&bars->p_full[st], ph) && mbar_test(&bars->v_full[st], ph)) {
+        tc_fence_after();
+        const uint32_t vb = sb + kOffV + st * kKVStage;
 #pragma unroll
-    for (int ks = 0; ks < kHD / 16; ++ks) {
-      const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
-      const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-      umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs
+          const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint64_t bdesc = smem_desc_sw128(vb + half * kKVHalf + ks * 2048, 1024, 1024);
+            umma_ts(tmem + kColO + half * 64, pa, bdesc, idesc_pv, jp > 0 || ks > 0);
+          }
+        }
+        umma_commit(&bars->v_empty[st]);
+        umma_commit(&bars->s_free[st]);  // P (in the S buffer) consumed; also marks this PV done
+        ++jp;
+        progressed = true;
+      }
     }
-    umma_commit(&bars->s_full[st]);
-    umma_commit(&bars->k_empty[st]);
-    if (j > 0 && !issue_pv(j - 1)) return false;
+    if (progressed) {
+      t_last = globaltimer_ns();
+    } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+      return false;
+    }
   }
-  return issue_pv(w.n_tiles - 1);
+  return true;
 }
 
 template <int N>
@@ -290,13 +308,13 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     // P (bf16 pairs) over this half's own S columns, which only this warp reads
     tmem_st16(taddr + st * 64 + hsel * 32, pk);
 
-    if (j > 0) {
-      // PV of the previous tile must be done before O is rescaled (and waiting on every phase
-      // keeps this barrier's parity in step)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (j - 1) & 1));
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      // O is rescaled only after the previous tile's PV is done (its S-buffer-free phase; that
+      // barrier cannot run a phase further ahead before this warp's P of this tile is posted)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
-      if (__any_sync(0xffffffffu, resc)) {
+      {
 #pragma unroll 1
         for (int ch = 0; ch < 2; ++ch) {
           float o[32];
@@ -327,10 +345,13 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->p_full);
+    if (lane == 0) mbar_arrive(&bars->p_full[st]);
   }
 
-  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (w.n_tiles - 1) & 1));
+  if (ok) {  // the last PV is done
+    const int jl = w.n_tiles - 1;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_free[jl & 1], (jl >> 1) & 1));
+  }
   if (!ok) {
     if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
     return;
@@ -393,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_free[s], 1);
     }
-    mbar_init(&bars->p_full, kSoftmaxWarps);
-    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->p_full[0], kSoftmaxWarps);
+    mbar_init(&bars->p_full[1], kSoftmaxWarps);
     fence_mbar_init();
     prefetch_tmap(&a.tm_q);
     prefetch_tmap(&a.tm_k);
