@@ -277,6 +277,32 @@ def run_ours(args, ws, rank, local):
     elapsed_ms = start.elapsed_time(stop)
     if flush is not None:  # exclude the flushes: the step is the span of its own operations
         elapsed_ms = sum(e[0].elapsed_time(e[3]) for e in evs)
+    eager_ms = elapsed_ms
+
+    if not args.eager:
+        # the same step captured once as a CUDA graph (the library allocates nothing and never
+        # synchronises inside a call) and replayed; per-kernel figures stay from the eager loop
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            step()
+        with torch.cuda.stream(st):
+            for _ in range(args.warmup):
+                g.replay()
+        torch.cuda.synchronize(dev)
+        barrier()
+        gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gclocks = ClockSampler(local)
+        gclocks.start()
+        time.sleep(0.3)
+        with torch.cuda.stream(st):
+            gs.record(st)
+            for _ in range(K):
+                g.replay()
+            ge.record(st)
+        torch.cuda.synchronize(dev)
+        barrier()
+        clk = gclocks.stop() or clk
+        elapsed_ms = gs.elapsed_time(ge)
     t_app = [e[0].elapsed_time(e[1]) for e in evs]
     t_dec = [e[1].elapsed_time(e[2]) for e in evs]
     t_ext = [e[2].elapsed_time(e[3]) for e in evs]
@@ -384,7 +410,9 @@ def run_ours(args, ws, rank, local):
             "l2": ("L2 flushed (256 MB written) before every step" if args.flush_l2 else
                    "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9)),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "launch": "eager launches" if args.eager else "CUDA graph of the whole step (per-kernel times from an eager pass)",
         },
+        "ms_per_step_eager": round(eager_ms / K, 4),
         "roofline": roofline,
         "kernels": kernels,
         "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
@@ -493,6 +521,10 @@ def load_workload(name):
         from workloads import make_config
 
         return make_config(WORKLOADS[name])
+    if name == "spec-verify":
+        from workloads import make_spec_verify
+
+        return make_spec_verify()
     if name == "profile":
         from workloads import random_small_batch
 
@@ -504,12 +536,14 @@ def load_workload(name):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="mixed", choices=sorted(WORKLOADS) + ["profile"])
+    ap.add_argument("--workload", default="mixed", choices=sorted(WORKLOADS) + ["spec-verify", "profile"])
     ap.add_argument("--flush-l2", action="store_true",
                     help="zero a 256 MB buffer before every timed step (for workloads that fit in L2); "
                          "the step time is then the sum of the per-operation event times")
     ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of the step captured as one CUDA graph")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)

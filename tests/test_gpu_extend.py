@@ -166,3 +166,17 @@ def test_extend_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
     assert e.value.status == 2  # group size 3
+
+
+def test_extend_speculative_verify_shape(lib):
+    """k drafted tokens + 1 verified in one extend over long contexts (sampled requests)."""
+    from workloads import make_spec_verify
+
+    b = make_spec_verify(num_requests=24, draft_tokens=5)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    out, lse = run_extend(lib, b, kp, vp)
+    sample = list(range(0, 24, 3))
+    o_ref, lse_ref = oracle_extend(b, kp, vp, requests=sample)
+    qo = b.ext_qo_indptr.tolist()
+    rows = [i for r in sample for i in range(qo[r], qo[r + 1])]
+    assert_attention_close(out, lse, o_ref, lse_ref, rows=rows, what="spec verify")

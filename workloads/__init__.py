@@ -14,4 +14,5 @@ from .paged import (  # noqa: F401
     make_config,
     CONFIG_NAMES,
     random_small_batch,
+    make_spec_verify,
 )

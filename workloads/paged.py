@@ -291,6 +291,19 @@ def make_config(idx: int) -> PagedBatch:
     raise ValueError(f"no workload {idx}")
 
 
+def make_spec_verify(num_requests: int = 64, draft_tokens: int = 5, seed: int = SEED_BASE + 6) -> PagedBatch:
+    """Target-model verification of speculative drafts: each request checks ``draft_tokens``
+    drafted tokens plus the bonus position in one extend of draft_tokens + 1 new tokens over its
+    cached context (Mini-SGLang README, "Speculative Decoding": k drafts verified in one parallel
+    prefill).  Context lengths U[512, 4096], Qwen3-8B attention shape, page 16."""
+    gen = torch.Generator().manual_seed(seed)
+    E = draft_tokens + 1
+    reqs = [RequestSpec("extend", _ri(gen, 512, 4096, 1)[0] + E, E) for _ in range(num_requests)]
+    return build_paged_batch(gen, reqs, name=f"speculative verify: {num_requests} requests x {E} tokens "
+                             "over contexts U[512,4096], 32q/8kv heads, D=128, page 16",
+                             page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128)
+
+
 def random_small_batch(
     seed: int,
     *,
