@@ -215,6 +215,16 @@ def run_ours(args, ws, rank, local):
     e_qo, e_ind, e_idx, e_pre = (b.ext_qo_indptr.to(dev), b.ext_kv_indptr.to(dev),
                                  b.ext_kv_indices.to(dev), b.ext_prefix_lens.to(dev))
     kn, vn, sm = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
+    if args.rope:
+        # the step's queries are the new tokens' (decodes first, then extend tokens, the slot
+        # order): one buffer the fused RoPE-append rotates in place, with decode/extend views
+        q_all = torch.cat([b.dec_q, b.ext_q]).to(dev)
+        dq, eq = q_all[: b.num_decode], q_all[b.num_decode:]
+        pos = []
+        for r in b.requests:
+            pos += list(range(r.kv_len - r.new_tokens, r.kv_len))
+        positions = torch.tensor(pos, dtype=torch.int32, device=dev)
+        table = pkv.rope_cos_sin_table(max(pos) + 1, b.head_dim, 1.0e6, device=dev)
     d_out = torch.empty_like(dq)
     d_lse = torch.empty((b.num_decode, b.num_q_heads), dtype=torch.float32, device=dev)
     e_out = torch.empty_like(eq)
@@ -230,7 +240,9 @@ def run_ours(args, ws, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(st)
-        if do_app:
+        if do_app and args.rope:
+            pkv.rope_kv_append(kp, vp, kn, vn, sm, positions, table, q=q_all, stream=st)
+        elif do_app:
             pkv.kv_append(kp, vp, kn, vn, sm, stream=st)
         if ev is not None:
             ev[1].record(st)
@@ -410,6 +422,7 @@ def run_ours(args, ws, rank, local):
             "l2": ("L2 flushed (256 MB written) before every step" if args.flush_l2 else
                    "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9)),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "append": "fused RoPE (theta 1e6) + KV append, queries rotated in place" if args.rope else "KV append",
             "launch": "eager launches" if args.eager else "CUDA graph of the whole step (per-kernel times from an eager pass)",
         },
         "ms_per_step_eager": round(eager_ms / K, 4),
@@ -542,6 +555,8 @@ def main():
                          "the step time is then the sum of the per-operation event times")
     ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="fuse the rotary embedding of the new K and of all queries into the append")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of the step captured as one CUDA graph")
     ap.add_argument("--gpus", type=int, default=1)

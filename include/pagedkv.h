@@ -87,6 +87,27 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
                          void* stream);
 
 /*
+ * KV-cache write fused with the rotary position embedding of the step's new tokens (the step
+ * just before attention in the engines' forward pass).  For t < num_tokens, with p = positions[t]:
+ *   pool.k row slot_mapping[t] = bf16(rope(k_new[t], p)),  pool.v row slot_mapping[t] = v_new[t],
+ *   and, when q is not NULL, q[t] = bf16(rope(q[t], p)) in place.
+ * rope is the half-split pairing of HF Llama/Qwen checkpoints (nanoSGLang README, "Notable
+ * Fixes"): for i < head_dim/2, x'[i] = x[i] cos a_i - x[i+D/2] sin a_i and
+ * x'[i+D/2] = x[i+D/2] cos a_i + x[i] sin a_i, computed in fp32 and rounded to nearest even.
+ *   cos_sin       fp32 [max_position, head_dim] (device): row p holds cos(a_i) in columns
+ *                 [0, D/2) and sin(a_i) in [D/2, D), a_i = p * theta^(-2i/D); built once by the caller
+ *   positions     int32 [num_tokens] (device); a position outside [0, max_position) skips that
+ *                 token's writes and reports PKV_DEVERR_LENGTH
+ *   q             nullable bf16 [num_tokens, num_q_heads, head_dim], rotated in place
+ *   slot_mapping, k_new, v_new, err_word as for pkv_kv_append.  head_dim a multiple of 16.
+ */
+pkv_status pkv_rope_kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, const int32_t* positions,
+                              const float* cos_sin, int32_t max_position, void* q,
+                              int32_t num_q_heads, int32_t num_tokens, uint32_t* err_word,
+                              void* stream);
+
+/*
  * Page gather (test and debug op): copy every request's K and V rows, in position order, into
  * contiguous buffers.  Request b occupies rows [sum_{b'<b} kv_lens[b'], ... + kv_lens[b]).
  *   kv_indptr  int32 [batch_size+1], kv_indices int32 [kv_indptr[batch_size]], kv_lens int32

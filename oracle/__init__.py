@@ -26,4 +26,7 @@ from .attention import (  # noqa: F401
     paged_extend,
     merge_states,
     decode_split_reference,
+    rope_angles,
+    rope,
+    rope_kv_append,
 )

@@ -291,3 +291,37 @@ def decode_split_reference(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, pa
         o[b], lse[b] = mo, ml
         partials.append((op, lp))
     return o, lse, partials
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding, half-split pairing (the rotate_half convention of HF Llama/Qwen
+# checkpoints, nanoSGLang README "Notable Fixes"), applied to K before it is written into the
+# pool and to Q before attention.
+# ---------------------------------------------------------------------------
+def rope_angles(positions, head_dim, theta):
+    """Angle of pair i at position p: p * theta**(-2i/D), fp64 ``[T, D/2]``."""
+    pos = np.asarray(positions, dtype=np.float64)
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / head_dim)
+    return pos[:, None] * inv_freq[None, :]
+
+
+def rope(x, positions, theta):
+    """Rotate x ``[T, H, D]`` (fp64) by the position of each token: for i < D/2,
+    x'[i] = x[i] cos a_i - x[i + D/2] sin a_i and x'[i + D/2] = x[i + D/2] cos a_i + x[i] sin a_i."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    ang = rope_angles(positions, D, theta)[:, None, :]  # [T, 1, D/2]
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., : D // 2], x[..., D // 2:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rope_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, positions, page_size, theta):
+    """KV write with RoPE applied to K: pool.k[slot[t]] = bf16(rope(k_new[t], pos[t])) (round to
+    nearest even from the fp64 rotation), pool.v[slot[t]] = v_new[t] bit-exact.  Negative slots
+    write nothing.  Returns (k_pool, v_pool, k_rot_f64) where k_rot_f64 is the unrounded rotation."""
+    k_rot = rope(as_f64(k_new), _as_int(positions), theta)
+    k_bf16 = torch.tensor(k_rot).to(torch.bfloat16) if torch is not None else k_rot
+    kp, vp = kv_append(k_pool, v_pool, k_bf16, v_new, slot_mapping, page_size)
+    return kp, vp, k_rot

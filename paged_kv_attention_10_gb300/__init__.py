@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
     "paged_decode", "extend_workspace_size", "paged_extend", "merge_states", "status_string",
-    "version", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT",
+    "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT",
     "DEVERR_INTERNAL",
 ]
 
@@ -73,6 +73,9 @@ def load():
         "pkv_paged_extend": (_c_i32, [P, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_i32,
                                       _c_f32, _vp, _vp, _vp, _c_sz, _vp, _vp]),
         "pkv_merge_states": (_c_i32, [_vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp]),
+        "pkv_rope_kv_append": (_c_i32, [P, _vp, _vp, _vp, _vp, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp]),
+        "pkv_paged_decode_noalloc": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
+                                              _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -149,6 +152,46 @@ def kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stream=
     with torch.cuda.device(dev):
         _call("pkv_kv_append", ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T,
               _ptr(err_word), _stream_ptr(stream, dev))
+
+
+def rope_cos_sin_table(max_position: int, head_dim: int, theta: float, device=None) -> torch.Tensor:
+    """The fp32 [max_position, head_dim] cos/sin table rope_kv_append reads: row p holds
+    cos(p * theta^(-2i/D)) for i < D/2, then the sines.  Built once, in fp64 on the host (large
+    positions keep full angle accuracy), like a model's rotary buffer."""
+    i = torch.arange(head_dim // 2, dtype=torch.float64)
+    inv_freq = theta ** (-2.0 * i / head_dim)
+    ang = torch.arange(max_position, dtype=torch.float64)[:, None] * inv_freq[None, :]
+    t = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
+    return t.to(device) if device is not None else t
+
+
+def rope_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, positions, cos_sin, q=None,
+                   err_word=None, stream=None) -> None:
+    """Rotate k_new (and q in place) by their positions and write K/V into the pool slots."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(k_new, "k_new", torch.bfloat16, dev)
+    _need(v_new, "v_new", torch.bfloat16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    _need(positions, "positions", torch.int32, dev)
+    _need(cos_sin, "cos_sin", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    T = slot_mapping.numel()
+    if k_new.shape != (T, pool.num_kv_heads, pool.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens, num_kv_heads, head_dim]")
+    if positions.numel() != T or cos_sin.dim() != 2 or cos_sin.shape[1] != pool.head_dim:
+        raise ValueError("positions must be [num_tokens] and cos_sin [max_position, head_dim]")
+    Hq = 0
+    if q is not None:
+        _need(q, "q", torch.bfloat16, dev)
+        if q.dim() != 3 or q.shape[0] != T or q.shape[2] != pool.head_dim:
+            raise ValueError("q must be [num_tokens, num_q_heads, head_dim]")
+        Hq = q.shape[1]
+    with torch.cuda.device(dev):
+        _call("pkv_rope_kv_append", ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+              _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], _ptr(q), Hq, T, _ptr(err_word),
+              _stream_ptr(stream, dev))
 
 
 def paged_gather(k_pool, v_pool, kv_indptr, kv_indices, kv_lens, total_len: int, err_word=None,

@@ -421,3 +421,70 @@ def test_pin_catches_missing_scale(monkeypatch):
     orig = oa.attend_rows
     monkeypatch.setattr(oa, "attend_rows", lambda q, K, V, vis, scale, rp=False: orig(q, K, V, vis, 1.0, rp))
     assert _pin_decode_bruteforce(6, [7], 2, 2, 16, 4) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# RoPE (half-split pairing)
+# ---------------------------------------------------------------------------
+def test_golden_rope():
+    c = GOLD["rope_quarter_turns"]
+    out = oracle.rope(np.array(c["x"], dtype=np.float64), c["positions"], c["theta"])
+    np.testing.assert_allclose(out, np.array(c["expect"]), rtol=0, atol=1e-15)
+
+
+def _rope_bruteforce(x, pos, theta):
+    """Explicit 2x2 rotation of each (i, i + D/2) pair, pure Python."""
+    D = len(x)
+    y = list(x)
+    for i in range(D // 2):
+        a = pos * theta ** (-2.0 * i / D)
+        c, s = math.cos(a), math.sin(a)
+        y[i] = c * x[i] - s * x[i + D // 2]
+        y[i + D // 2] = s * x[i] + c * x[i + D // 2]
+    return y
+
+
+def test_rope_matches_explicit_rotation():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((5, 3, 16))
+    pos = [0, 1, 17, 4095, 32767]
+    out = oracle.rope(x, pos, 1e6)
+    for t in range(5):
+        for h in range(3):
+            ref = _rope_bruteforce(x[t, h].tolist(), pos[t], 1e6)
+            assert np.abs(np.array(ref) - out[t, h]).max() < 1e-12
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(1)
+    D = 128
+    q = rng.standard_normal((1, 1, D))
+    k = rng.standard_normal((1, 1, D))
+    # position 0 is the identity; each pair keeps its norm
+    assert np.array_equal(oracle.rope(q, [0], 1e4), q)
+    r = oracle.rope(q, [777], 1e4)[0, 0]
+    assert np.allclose(r[: D // 2] ** 2 + r[D // 2:] ** 2, q[0, 0, : D // 2] ** 2 + q[0, 0, D // 2:] ** 2, atol=1e-12)
+    # scores depend only on the relative position
+    for m, n in ((10, 3), (5000, 4993), (2, 9)):
+        a = oracle.rope(q, [m], 1e4)[0, 0] @ oracle.rope(k, [n], 1e4)[0, 0]
+        b = oracle.rope(q, [m - n], 1e4)[0, 0] @ k[0, 0]
+        assert abs(a - b) < 1e-9
+
+
+def test_pin_catches_interleaved_rope(monkeypatch):
+    """The adjacent-pair (interleaved) convention is a different rotation: the golden case sees it."""
+    def interleaved(x, positions, theta):
+        x = np.asarray(x, dtype=np.float64)
+        D = x.shape[-1]
+        ang = oa.rope_angles(positions, D, theta)[:, None, :]
+        c, s = np.cos(ang), np.sin(ang)
+        ev, od = x[..., 0::2], x[..., 1::2]
+        y = np.empty_like(x)
+        y[..., 0::2] = ev * c - od * s
+        y[..., 1::2] = od * c + ev * s
+        return y
+
+    monkeypatch.setattr(oa, "rope", interleaved)
+    c = GOLD["rope_quarter_turns"]
+    out = oa.rope(np.array(c["x"], dtype=np.float64), c["positions"], c["theta"])
+    assert np.abs(out - np.array(c["expect"])).max() > 0.1
