@@ -13,8 +13,10 @@
 //    loaded is used by the whole group.  Q arrives by one 3-D TMA box per 64-column half.
 //  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
 //    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
-//  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=2x64, K=64) run as tcgen05.mma issued
+//  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=128, K=64) run as tcgen05.mma issued
 //    by one thread, accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.
+//    A tcgen05.mma issue costs about as long as an N=128 MMA whatever its N, so PV is issued as
+//    one N=128 MMA per 16 positions rather than two of N=64.
 //    P is written back as bf16 pairs over the S columns it came from and the PV MMA reads it from
 //    TMEM, so P never passes through shared memory.
 //  * Eight softmax warps, two per TMEM lane quadrant: a thread owns one row and one half of the
@@ -158,7 +160,7 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
 // behind a QK whose S buffer is not yet free (and the reverse).
 __device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
   constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
-  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, 64, true);
+  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, kHD, true);
   if (!mbar_wait(&bars->q_full, 0)) return false;
   const int n = w.n_tiles;
   int jq = 0, jp = 0;
@@ -191,13 +193,12 @@ __device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_
         const uint32_t vb = sb + kOffV + st * kKVStage;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs
+          // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs.
+          // V rows [16ks, 16ks+16) as one MN-major operand of N = 128; its two 64-dim halves are
+          // kKVHalf apart.
           const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint64_t bdesc = smem_desc_sw128(vb + half * kKVHalf + ks * 2048, 1024, 1024);
-            umma_ts(tmem + kColO + half * 64, pa, bdesc, idesc_pv, jp > 0 || ks > 0);
-          }
+          const uint64_t bdesc = smem_desc_sw128(vb + ks * 2048, kKVHalf, 1024);
+          umma_ts(tmem + kColO, pa, bdesc, idesc_pv, jp > 0 || ks > 0);
         }
         umma_commit(&bars->v_empty[st]);
         umma_commit(&bars->s_free[st]);  // P (in the S buffer) consumed; also marks this PV done
