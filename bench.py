@@ -474,9 +474,13 @@ def _oracle_sample_runner(b, kp, vp):
     return run
 
 
-def cpu_baseline(b, seconds=12.0):
+def cpu_baseline(b, seconds=12.0, threads=0):
+    import torch as _t
+
     import oracle
 
+    cores = threads if threads > 0 else len(os.sched_getaffinity(0))
+    _t.set_num_threads(cores)
     kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
     run = _oracle_sample_runner(b, kp, vp)
     t0 = time.perf_counter()
@@ -485,11 +489,10 @@ def cpu_baseline(b, seconds=12.0):
         toks += run(k)
         k += 1
     el = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0))
     return {"value": round(toks / el, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{k} slices of the workload, each 1 decode request (all heads) and/or up to 8 "
                       f"extend query rows of one request; {toks} attention tokens in {el:.1f} s; fp64 NumPy, "
-                      f"BLAS may use all {cores} affinity cores"}
+                      f"BLAS and torch limited to {cores} threads"}
 
 
 def run_reference(args, ws, rank):
@@ -565,7 +568,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="threads the CPU oracle may use (default: every affinity core)")
     args = ap.parse_args()
+    if args.cpu_threads > 0:  # before NumPy or torch start their thread pools
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = str(args.cpu_threads)
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = _dist_env()
@@ -583,7 +591,8 @@ def main():
     line = run_ours(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(load_workload(args.workload), args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(load_workload(args.workload), args.cpu_seconds,
+                                                args.cpu_threads)
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
