@@ -13,8 +13,10 @@
 //    loaded is used by the whole group.  Q arrives by one 3-D TMA box per 64-column half.
 //  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
 //    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
-//  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=128, K=64) run as tcgen05.mma issued
-//    by one thread, accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.
+//  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=128, K=64) run as tcgen05.mma,
+//    accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.  QK and PV are
+//    issued by two threads in different warps, each blocked in a try_wait on its own operands, so
+//    a PV whose P is ready starts within a few hundred cycles instead of waiting behind a QK.
 //    A tcgen05.mma issue costs about as long as an N=128 MMA whatever its N, so PV is issued as
 //    one N=128 MMA per 16 positions rather than two of N=64.
 //    P is written back as bf16 pairs over the S columns it came from and the PV MMA reads it from
@@ -35,7 +37,8 @@ using namespace pkv;
 constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
 constexpr int kBN = 64;   // KV positions per tile
 constexpr int kHD = 128;  // head_dim
-constexpr int kThreads = 352;  // warp 0 Q/K loads, warp 1 MMA, warps 2..9 softmax, warp 10 V loads
+// warp 0 Q/K loads, warp 1 QK MMAs, warps 2..9 softmax, warp 10 V loads, warp 11 PV MMAs
+constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 256); S buffers at [0,64) and [64,128)
@@ -57,6 +60,7 @@ struct Bars {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2];  // S buffer b: QK written / its P consumed by PV
   uint64_t p_full[2];              // P of the tile in S buffer b written by the softmax
+  uint64_t qk_done, pv_done;       // every MMA of the issuing thread has completed (exit path)
   uint32_t tmem_base;
   uint32_t pad;
 };
@@ -154,63 +158,52 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   return true;
 }
 
-// One thread issues all MMAs.  QK of tile jq (into S buffer jq&1) needs the K tile and the S
-// buffer back from the PV two tiles earlier; PV of tile jp needs the softmax's P and the V tile.
-// The two streams are polled with non-blocking tests, so a PV whose P is ready never waits
-// behind a QK whose S buffer is not yet free (and the reverse).
-__device__ bool extend_mma(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
+// The MMAs are issued by two threads, one per stream, each waiting with a blocking try_wait that
+// wakes when its phase completes:  the QK thread issues QK(j) once K(j) has landed and S buffer
+// j&1 is back from PV(j-2) (P is written over S);  the PV thread issues PV(j) once the softmax
+// has written P(j) and V(j) has landed.  Neither stream ever waits behind the other.
+__device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
   constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
-  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, kHD, true);
   if (!mbar_wait(&bars->q_full, 0)) return false;
-  const int n = w.n_tiles;
-  int jq = 0, jp = 0;
-  uint64_t t_last = globaltimer_ns();
-  while (jp < n) {
-    bool progressed = false;
-    if (jq < n && jq < jp + 2) {
-      const int st = jq & 1;
-      const uint32_t ph = (jq >> 1) & 1;
-      if (mbar_test(&bars->k_full[st], ph) && mbar_test(&bars->s_free[st], ph ^ 1)) {
-        tc_fence_after();
-        const uint32_t kb = sb + kOffK + st * kKVStage;
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    const uint32_t ph = (j >> 1) & 1;
+    if (!mbar_wait(&bars->k_full[st], ph)) return false;
+    if (!mbar_wait(&bars->s_free[st], ph ^ 1)) return false;
+    tc_fence_after();
+    const uint32_t kb = sb + kOffK + st * kKVStage;
 #pragma unroll
-        for (int ks = 0; ks < kHD / 16; ++ks) {
-          const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-          umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
-        }
-        umma_commit(&bars->s_full[st]);
-        umma_commit(&bars->k_empty[st]);
-        ++jq;
-        progressed = true;
-      }
+    for (int ks = 0; ks < kHD / 16; ++ks) {
+      const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+      const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+      umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
     }
-    if (jp < jq) {
-      const int st = jp & 1;
-      const uint32_t ph = (jp >> 1) & 1;
-      if (mbar_test(&bars->p_full[st], ph) && mbar_test(&bars->v_full[st], ph)) {
-        tc_fence_after();
-        const uint32_t vb = sb + kOffV + st * kKVStage;
+    umma_commit(&bars->s_full[st]);
+    umma_commit(&bars->k_empty[st]);
+  }
+  return true;
+}
+
+__device__ bool extend_mma_pv(Bars* bars, uint32_t sb, uint32_t tmem, const Work& w) {
+  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, kHD, true);
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    const uint32_t ph = (j >> 1) & 1;
+    if (!mbar_wait(&bars->p_full[st], ph)) return false;
+    if (!mbar_wait(&bars->v_full[st], ph)) return false;
+    tc_fence_after();
+    const uint32_t vb = sb + kOffV + st * kKVStage;
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs.
-          // V rows [16ks, 16ks+16) as one MN-major operand of N = 128; its two 64-dim halves are
-          // kKVHalf apart.
-          const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
-          const uint64_t bdesc = smem_desc_sw128(vb + ks * 2048, kKVHalf, 1024);
-          umma_ts(tmem + kColO, pa, bdesc, idesc_pv, jp > 0 || ks > 0);
-        }
-        umma_commit(&bars->v_empty[st]);
-        umma_commit(&bars->s_free[st]);  // P (in the S buffer) consumed; also marks this PV done
-        ++jp;
-        progressed = true;
-      }
+    for (int ks = 0; ks < kBN / 16; ++ks) {
+      // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs.
+      // V rows [16ks, 16ks+16) as one MN-major operand of N = 128; its two 64-dim halves are
+      // kKVHalf apart.
+      const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
+      const uint64_t bdesc = smem_desc_sw128(vb + ks * 2048, kKVHalf, 1024);
+      umma_ts(tmem + kColO, pa, bdesc, idesc_pv, j > 0 || ks > 0);
     }
-    if (progressed) {
-      t_last = globaltimer_ns();
-    } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
-      return false;
-    }
+    umma_commit(&bars->v_empty[st]);
+    umma_commit(&bars->s_free[st]);  // P (in the S buffer) consumed; also marks this PV done
   }
   return true;
 }
@@ -415,6 +408,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_free[s], 1);
     }
+    mbar_init(&bars->qk_done, 1);
+    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->p_full[0], kSoftmaxWarps);
     mbar_init(&bars->p_full[1], kSoftmaxWarps);
     fence_mbar_init();
@@ -434,7 +429,19 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   if (warp == 0 || warp == 10) {
     extend_producer(a, sb, bars, w, warp == 0 ? 0 : 1);
   } else if (warp == 1) {
-    if (lane == 0 && !extend_mma(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) {
+      if (!extend_mma_qk(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      // its MMAs have completed before TMEM is released (immediate on the normal path)
+      umma_commit(&bars->qk_done);
+      if (!mbar_wait(&bars->qk_done, 0)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    if (lane == 0) {
+      if (!extend_mma_pv(bars, sb, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      umma_commit(&bars->pv_done);
+      if (!mbar_wait(&bars->pv_done, 0)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    }
     __syncwarp();
   } else {
     extend_softmax(a, smem, bars, tmem, w);
