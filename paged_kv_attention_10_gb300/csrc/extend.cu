@@ -217,6 +217,11 @@ __device__ __forceinline__ float tree_max(float (&v)[N]) {
   return v[0];
 }
 
+// barrier of all eight softmax warps (id 5)
+__device__ __forceinline__ void softmax_bar() {
+  asm volatile("bar.sync 5, 256;" ::: "memory");
+}
+
 // barrier shared by the two softmax warps of TMEM lane quadrant wq (ids 1..4)
 __device__ __forceinline__ void pair_bar(int wq) {
   switch (wq) {
@@ -357,23 +362,41 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   pair_bar(wq);
   const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
   const float inv = 1.f / l_tot;
-  const int64_t row = (int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g;
-  uint4* orow = reinterpret_cast<uint4*>(a.out + row * kHD + hsel * 64);
+  // The normalised O tile goes through shared memory so that the stores to `out` are coalesced
+  // (a thread owns one row; storing rows directly scatters every warp store over 32 rows).  The
+  // Q buffer is free: every QK has completed.  Row r's 16-byte chunk c sits at chunk c ^ (r % 16)
+  // of its 256-byte line, which spreads a warp's column of chunks over the banks.
+  uint8_t* stage = smem + kOffQ;
 #pragma unroll 1
   for (int ch = 0; ch < 2; ++ch) {
     float o[32];
     tmem_ld32(taddr + kColO + hsel * 64 + ch * 32, o);
     tmem_wait_ld();
-    if (valid) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        orow[ch * 4 + q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                      pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                      pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                      pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+    for (int q = 0; q < 4; ++q) {
+      const int c = hsel * 8 + ch * 4 + q;
+      *reinterpret_cast<uint4*>(stage + r * 256 + ((c ^ (r & 15)) << 4)) =
+          make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                     pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                     pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                     pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
     }
   }
-  if (valid && hsel == 0 && a.lse) a.lse[row] = (m_used + log2f(l_tot)) * kLn2;
+  if (valid && hsel == 0 && a.lse)
+    a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l_tot)) * kLn2;
+  softmax_bar();
+  // 128 rows x 16 chunks: a warp stores two whole 256-byte rows per instruction
+#pragma unroll
+  for (int k = 0; k < kBM * 16 / (kSoftmaxWarps * 32); ++k) {
+    const int i = tid + k * kSoftmaxWarps * 32;
+    const int row = i >> 4, c = i & 15;
+    const int t = w.t0 + (row >> a.log2_group);
+    if (t < w.E) {
+      const int64_t orow = (int64_t)(w.qo0 + t) * a.num_q_heads + (int64_t)w.h * G + (row & (G - 1));
+      reinterpret_cast<uint4*>(a.out + orow * kHD)[c] =
+          *reinterpret_cast<const uint4*>(stage + row * 256 + ((c ^ (row & 15)) << 4));
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
