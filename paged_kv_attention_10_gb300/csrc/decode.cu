@@ -26,6 +26,7 @@
 #include <float.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "tc05.cuh"
 
@@ -639,31 +640,58 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
     if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
     return;
   }
+  // Every load below is independent of the others in its group, so the merge costs a few L2 round
+  // trips whatever the number of partials: the max over all partials' LSE (256 per group), then
+  // their weights (read-only-cache hits) and 16 partial rows per lane in flight.
+  const float* plse = a.part_lse + qhl;
   float mx = -INFINITY;
-  for (int p = first + lane; p <= last; p += 32) mx = fmaxf(mx, a.part_lse[(int64_t)p * HQU + qhl]);
+  for (int base = first; base <= last; base += 256) {
+    float lv[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int p = base + 32 * c + lane;
+      lv[c] = p <= last ? __ldg(plse + (int64_t)p * HQU) : -INFINITY;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) mx = fmaxf(mx, lv[c]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  using VecT = typename std::conditional<VPL == 4, float4, float2>::type;
   float acc[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
   float tot = 0.f;
-  for (int p0 = first; p0 <= last; p0 += 32) {
-    const int p = p0 + lane;
-    const float w = p <= last ? __expf(a.part_lse[(int64_t)p * HQU + qhl] - mx) : 0.f;
-    tot += warp_sum(w);
-    const int n = min(32, last - p0 + 1);
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, w, i);
-      const float* pp = a.part_o + ((int64_t)(p0 + i) * HQU + qhl) * D + lane * VPL;
+  const float* po = a.part_o + (int64_t)qhl * D + lane * VPL;
+  for (int base = first; base <= last; base += 32) {
+    const int n = min(32, last - base + 1);
+    const float w = lane < n ? __expf(__ldg(plse + (int64_t)(base + lane) * HQU) - mx) : 0.f;
+    tot += w;
+    for (int i0 = 0; i0 < n; i0 += 16) {
+      VecT x[16];
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) acc[v] += wi * pp[v];
+      for (int k = 0; k < 16; ++k) {
+        x[k] = i0 + k < n ? __ldg(reinterpret_cast<const VecT*>(po + (int64_t)(base + i0 + k) * HQU * D))
+                          : VecT{};
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, (i0 + k) & 31);
+        const float* xv = reinterpret_cast<const float*>(&x[k]);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) acc[v] += wk * xv[v];
+      }
     }
   }
+  tot = warp_sum(tot);
   const float inv = 1.f / tot;
   __nv_bfloat16* op = a.out + ((int64_t)b * a.num_q_heads + qh) * D + lane * VPL;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) op[i] = __float2bfloat16_rn(acc[i] * inv);
+  if constexpr (VPL == 4) {
+    *reinterpret_cast<uint2*>(op) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                               pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(op) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
   if (lane == 0 && a.lse) a.lse[(int64_t)b * a.num_q_heads + qh] = mx + logf(tot);
 }
 
