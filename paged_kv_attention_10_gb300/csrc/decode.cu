@@ -107,13 +107,18 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   const uint32_t region = a.kv_region;
   // bytes one 16-token slice brings in (K and V) on the TMA path
   const uint32_t slice_bytes = (uint32_t)(D / 64) * a.HC * 16 * 128 * 2;
-  // Page indices come from a register window of 64 consecutive page-list entries (two 32-lane
-  // halves) whose upper half is loaded 32 pages before it is needed, so the copies of a stage
-  // never wait on a global load.  Usable when one stage spans at most 33 pages.
+  // Page indices come from a register window of 96 consecutive page-list entries (three 32-lane
+  // slices).  A stage reads only the first 64; the third slice is loaded when the window moves,
+  // 32 pages before any stage can need it, so the copies of a stage never wait on a global load
+  // even when a stage spans 16 pages (page size 1).  Usable when one stage spans at most 33 pages.
   const bool windowed = (Ts - 1) / ps + 2 <= 32;
 
   int64_t sumS = 0;  // 16-token slices over all requests
-  for (int i = lane; i < a.batch; i += 32) sumS += (max(0, __ldg(a.kv_lens + i)) + 15) / 16;
+  for (int i = lane; i < a.batch; i += 32) {
+    // the walk below reads the page-list offsets next: bring them to L2 meanwhile
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.kv_indptr + i));
+    sumS += (max(0, __ldg(a.kv_lens + i)) + 15) / 16;
+  }
   sumS = warp_sum(sumS);
   const int64_t T = sumS * nhg;
   int64_t share = (T + gridDim.x - 1) / gridDim.x;
@@ -127,13 +132,13 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
 
   int32_t cur_p0 = 0, cur_p1 = 0;  // page list of the request being streamed
   int win_b = -1, wbase = 0;
-  int32_t w0 = -1, w1 = -1;
+  int32_t w0 = -1, w1 = -1, w2 = -1;
 
   auto entry = [&](int pidx) -> int32_t {  // page-list entry pidx of the current request; -1 past its end
     const int64_t s = (int64_t)cur_p0 + pidx;
     return (pidx >= 0 && s < cur_p1) ? __ldg(a.kv_indices + s) : -1;
   };
-  auto window_page = [&](int pidx) -> int32_t {  // all lanes must call
+  auto window_page = [&](int pidx) -> int32_t {  // all lanes must call; pidx - wbase < 64
     const int k = pidx - wbase;
     const int32_t v0 = __shfl_sync(0xffffffffu, w0, k & 31);
     const int32_t v1 = __shfl_sync(0xffffffffu, w1, k & 31);
@@ -148,6 +153,13 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
   };
 
   auto emit = [&](int unit, int b, int hg, int tok0, int ntok, int flags) -> bool {
+    if (unit >= 0 && (flags & kSegFirst)) {
+      // the consumers read this unit's queries when its first stage lands: bring them to L2 now
+      const int hqu = a.HC * a.group;
+      const char* qb = reinterpret_cast<const char*>(a.q + ((int64_t)b * a.num_q_heads + (int64_t)hg * hqu) * D);
+      for (int off = lane * 128; off < hqu * D * 2; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
+    }
     if (unit >= 0 && windowed) {
       const int first_page = tok0 / ps;
       if (b != win_b || first_page < wbase) {  // new request or restart from its first page
@@ -155,11 +167,13 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
         wbase = first_page;
         w0 = entry(wbase + lane);
         w1 = entry(wbase + 32 + lane);
+        w2 = entry(wbase + 64 + lane);
       }
       while (first_page >= wbase + 32) {
         w0 = w1;
+        w1 = w2;
         wbase += 32;
-        w1 = entry(wbase + 32 + lane);
+        w2 = entry(wbase + 64 + lane);
       }
     }
     if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -381,15 +395,27 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
     const int nv = min(16, h.ntok - si * 16);
     const uint32_t kb = stages_u32 + (uint32_t)stage * 2 * region;
     const uint32_t vb = kb + region;
-    if (TMA && nv > 0 && nv < 16) {
-      // a partial slice: the TMA box also brought rows past the request's end (unused slots,
-      // possibly NaN); zero this head's V rows there so that P = 0 times V stays 0
-      uint8_t* vrow = stages + (size_t)stage * 2 * region + region + si * HC * 2048 + hl * 2048;
-      for (int idx = lane; idx < (16 - nv) * 8 * (D / 64); idx += 32) {
-        const int hf = idx / ((16 - nv) * 8);
-        const int rem = idx - hf * (16 - nv) * 8;
-        *reinterpret_cast<uint4*>(vrow + hf * half_stride + (nv + (rem >> 3)) * 128 + (rem & 7) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+    if (nv > 0 && nv < 16) {
+      // a partial slice: the rows past the request's end hold unused pool slots (the TMA box
+      // brings them, possibly NaN) or whatever shared memory held before (the row copies skip
+      // them); zero this head's V rows there so that P = 0 times V stays 0.  K rows there are
+      // masked by a select, so their contents never matter.
+      uint8_t* vreg = stages + (size_t)stage * 2 * region + region;
+      if (TMA) {
+        uint8_t* vrow = vreg + si * HC * 2048 + hl * 2048;
+        for (int idx = lane; idx < (16 - nv) * 8 * (D / 64); idx += 32) {
+          const int hf = idx / ((16 - nv) * 8);
+          const int rem = idx - hf * (16 - nv) * 8;
+          *reinterpret_cast<uint4*>(vrow + hf * half_stride + (nv + (rem >> 3)) * 128 + (rem & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+        constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of one head's row
+        for (int idx = lane; idx < (16 - nv) * kChunks; idx += 32) {
+          const int row = si * 16 + nv + idx / kChunks;
+          *reinterpret_cast<uint4*>(vreg + (size_t)row * RS + hl * D * 2 + (idx % kChunks) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       __syncwarp();
     }
@@ -466,7 +492,7 @@ __device__ void decode_consumer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
         for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
       }
     }
-    if (TMA && nv > 0 && nv < 16) fence_proxy_async_smem();  // zeros above, before the next TMA fill
+    if (nv > 0 && nv < 16) fence_proxy_async_smem();  // zeros above, before the next async fill
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
 
@@ -582,9 +608,6 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const __grid_const
   uint64_t* empty = full + NS;
   float* mbuf = reinterpret_cast<float*>(empty + NS);
 
-  // rows that no copy writes (the tail of a partial slice) must hold finite values
-  for (size_t i = threadIdx.x; i < stage_region / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(stages)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
