@@ -19,9 +19,10 @@ import torch
 
 __all__ = [
     "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
-    "paged_decode", "extend_workspace_size", "paged_extend", "merge_states", "status_string",
-    "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT",
-    "DEVERR_INTERNAL",
+    "paged_decode", "paged_decode_noalloc", "extend_workspace_size", "paged_extend",
+    "merge_states", "status_string",
+    "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB",
+    "DEVERR_LENGTH", "DEVERR_TIMEOUT", "DEVERR_INTERNAL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -243,6 +244,32 @@ def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: fl
         _call("pkv_paged_decode", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
               _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
               _ptr(workspace), workspace.numel(), _ptr(err_word), _stream_ptr(stream, dev))
+    return out, lse
+
+
+def paged_decode_noalloc(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: float,
+                         out=None, lse=None, err_word=None, stream=None, return_lse=True):
+    """paged_decode with the split partials in the library's own device scratch (no workspace
+    argument, nothing allocated per call). Returns (out, lse)."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(q, "q", torch.bfloat16, dev)
+    for t, n in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (kv_lens, "kv_lens")):
+        _need(t, n, torch.int32, dev)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    with torch.cuda.device(dev):
+        _call("pkv_paged_decode_noalloc", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
+              _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse), _ptr(err_word),
+              _stream_ptr(stream, dev))
     return out, lse
 
 

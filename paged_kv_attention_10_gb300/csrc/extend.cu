@@ -12,7 +12,8 @@
 //    128/G consecutive tokens times the G query heads that share the KV head, so each K/V tile
 //    loaded is used by the whole group.  Q arrives by one 3-D TMA box per 64-column half.
 //  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
-//    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into a 2-stage ring.
+//    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into 2-stage rings filled by
+//    two producer warps (K with Q, and V), so the K stream runs ahead of the V stream.
 //  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=128, K=64) run as tcgen05.mma,
 //    accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.  QK and PV are
 //    issued by two threads in different warps, each blocked in a try_wait on its own operands, so
@@ -25,7 +26,7 @@
 //    tile's columns.  The two halves of a row exchange partial maxima through shared memory, apply
 //    the causal mask and the online softmax in fp32 (the running max only moves when it grows by
 //    more than 2^8, so O is rescaled in TMEM rarely), and finally normalise their halves of the O
-//    row and store them.
+//    row into a shared-memory tile that all eight warps copy out with coalesced stores.
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include "tc05.cuh"
@@ -95,7 +96,8 @@ struct Work {
 // page indices come from a register window of 64 page-list entries whose upper half is loaded
 // 32 pages before it is needed, so no TMA waits on a dependent global load.
 // kv = 0: the K warp (also loads Q); kv = 1: the V warp.  Separate warps keep the K stream
-// ahead of the QK MMAs even while the V stream waits for its stage to be freed by PV.
+// ahead of the QK MMAs even while the V stream waits for its stage to be freed by PV.  The
+// warp returns only when its copies have landed (bounded waits).
 __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
   const int lane = threadIdx.x & 31;
   const int G = a.group;
@@ -111,8 +113,13 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   auto entry = [&](int pidx) -> int32_t {
     return (pidx >= 0 && pidx < np) ? __ldg(a.kv_indices + p0 + pidx) : -1;
   };
+  uint64_t* fulls = kv ? bars->v_full : bars->k_full;
+  uint64_t* empties = kv ? bars->v_empty : bars->k_empty;
+  const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
   int wbase = 0;
   int32_t w0 = entry(lane), w1 = entry(32 + lane);
+  int issued = 0;
+  bool ok = true;
   for (int j = 0; j < w.n_tiles; ++j) {
     const int st = j & 1;
     const uint32_t ph = (j >> 1) & 1;
@@ -138,24 +145,25 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
         row = (int)((int64_t)page * a.page_size + (pos0 & (a.page_size - 1)));
     }
     const uint32_t nload = __popc(__ballot_sync(0xffffffffu, row >= 0));
-    {
-      uint64_t* empty = kv ? &bars->v_empty[st] : &bars->k_empty[st];
-      uint64_t* full = kv ? &bars->v_full[st] : &bars->k_full[st];
-      const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
-      if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1))) {
-        if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
-        return false;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(full, nload * R * 128 * 2);
-      __syncwarp();
-      if (row >= 0) {
-        const uint32_t dst = sb + (kv ? kOffV : kOffK) + st * kKVStage + lane * R * 128;
-        tma_load_3d(dst, tm, 0, w.h, row, full);
-        tma_load_3d(dst + kKVHalf, tm, 64, w.h, row, full);
-      }
+    if (!__all_sync(0xffffffffu, mbar_wait(&empties[st], ph ^ 1))) {
+      if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      ok = false;
+      break;
     }
+    if (lane == 0) mbar_arrive_expect_tx(&fulls[st], nload * R * 128 * 2);
+    __syncwarp();
+    if (row >= 0) {
+      const uint32_t dst = sb + (kv ? kOffV : kOffK) + st * kKVStage + lane * R * 128;
+      tma_load_3d(dst, tm, 0, w.h, row, &fulls[st]);
+      tma_load_3d(dst + kKVHalf, tm, 64, w.h, row, &fulls[st]);
+    }
+    issued = j + 1;
   }
-  return true;
+  // no copy of this warp is in flight when the CTA exits, also after a timeout elsewhere
+  // (immediate on the normal path, where the MMAs have consumed every tile)
+  for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&fulls[j & 1], (j >> 1) & 1);
+  if (kv == 0) mbar_wait(&bars->q_full, 0);
+  return ok;
 }
 
 // The MMAs are issued by two threads, one per stream, each waiting with a blocking try_wait that

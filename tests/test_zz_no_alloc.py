@@ -108,3 +108,16 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(cdll):
     st = cdll.pkv_paged_decode_noalloc(ctypes.byref(pool), _p(dummy), B, hq, _p(dummy), _p(dummy),
                                        _p(dummy), 1.0, _p(dummy), None, None, None)
     assert st == 3  # PKV_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_binding_matches_paged_decode(lib):
+    # the same entry point through the Python binding, against the workspace decode
+    b, t, pool = _device_batch(43, (1500, 64, 777))
+    out_ref, lse_ref = lib.paged_decode(t["q"], t["kp"], t["vp"], t["ind"], t["idx"], t["lens"],
+                                        b.sm_scale)
+    out, lse = lib.paged_decode_noalloc(t["q"], t["kp"], t["vp"], t["ind"], t["idx"], t["lens"],
+                                        b.sm_scale)
+    torch.cuda.synchronize()
+    d = (out.float() - out_ref.float()).abs()
+    assert d.max().item() <= O_MAX_ABS and d.mean().item() <= O_MEAN_ABS
+    assert (lse - lse_ref).abs().max().item() <= LSE_ABS
