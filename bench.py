@@ -257,6 +257,40 @@ def run_ours(args, ws, rank, local):
         if ev is not None:
             ev[3].record(st)
 
+    # The same step as two branches that share no data: the decodes' new tokens then decode (and
+    # its split merge), beside the extend chunks' new tokens then extend.  New tokens are laid out
+    # request by request with the decodes first, so each branch appends a contiguous range.  The
+    # extend's append then runs during the decode, and extend CTAs take SMs as decode CTAs finish.
+    nd_new = sum(r.new_tokens for r in b.requests if r.kind == "decode")
+    decodes_first = all(r.kind == "decode" for r in b.requests[: b.num_decode])
+    overlap = (do_app and do_dec and do_ext and decodes_first and not args.serial_step
+               and (not args.rope or nd_new == b.num_decode))
+    st2 = torch.cuda.Stream(device=dev)
+    fork_ev, join_ev = torch.cuda.Event(), torch.cuda.Event()
+
+    def append_range(lo, hi, stream):
+        if hi <= lo:
+            return
+        if args.rope:
+            pkv.rope_kv_append(kp, vp, kn[lo:hi], vn[lo:hi], sm[lo:hi], positions[lo:hi], table,
+                               q=q_all[lo:hi], stream=stream)
+        else:
+            pkv.kv_append(kp, vp, kn[lo:hi], vn[lo:hi], sm[lo:hi], stream=stream)
+
+    def step_branches():
+        fork_ev.record(st)
+        st2.wait_event(fork_ev)
+        append_range(0, nd_new, st)
+        pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
+                         workspace=dws, stream=st)
+        append_range(nd_new, kn.shape[0], st2)
+        pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
+                         lse=e_lse, stream=st2)
+        join_ev.record(st2)
+        st.wait_event(join_ev)
+
+    whole_step = step_branches if overlap else step
+
     def barrier():
         if ws > 1:
             dist.barrier()
@@ -296,7 +330,7 @@ def run_ours(args, ws, rank, local):
         # synchronises inside a call) and replayed; per-kernel figures stay from the eager loop
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=st):
-            step()
+            whole_step()
         with torch.cuda.stream(st):
             for _ in range(args.warmup):
                 g.replay()
@@ -339,7 +373,7 @@ def run_ours(args, ws, rank, local):
     def e2e_step():
         for n, t in host_in.items():
             dev_in[n].copy_(t, non_blocking=True)
-        step()
+        whole_step()
         for n, t in host_out.items():
             t.copy_(dev_out[n], non_blocking=True)
 
@@ -423,7 +457,10 @@ def run_ours(args, ws, rank, local):
                    "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9)),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "append": "fused RoPE (theta 1e6) + KV append, queries rotated in place" if args.rope else "KV append",
-            "launch": "eager launches" if args.eager else "CUDA graph of the whole step (per-kernel times from an eager pass)",
+            "launch": ("eager launches" if args.eager else "CUDA graph of the whole step")
+            + ("; two branches: (append of the decodes' tokens, decode, merge) beside (append of the "
+               "extend tokens, extend)" if overlap else "; one stream")
+            + " (per-kernel times from an eager pass on one stream)",
         },
         "ms_per_step_eager": round(eager_ms / K, 4),
         "roofline": roofline,
@@ -562,6 +599,8 @@ def main():
                     help="fuse the rotary embedding of the new K and of all queries into the append")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of the step captured as one CUDA graph")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="run the step's operations one after another on one stream (no branches)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)

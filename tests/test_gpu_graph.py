@@ -71,3 +71,69 @@ def test_captured_step_matches_eager_and_oracle(lib):
     o_ref, l_ref = oracle.paged_extend(b2.ext_q, kp, vp, b2.ext_qo_indptr, b2.ext_kv_indptr,
                                        b2.ext_kv_indices, b2.ext_prefix_lens, 16, b2.sm_scale)
     assert_attention_close(e_out, e_lse, o_ref, l_ref, what="graph extend")
+
+
+def test_two_branch_step_matches_serial_and_oracle(lib):
+    # The step as two graph branches that share no data (the decodes' new tokens, then decode and
+    # its merge, beside the extend tokens, then extend), as the benchmark captures it: the same
+    # bits as the serial step, and the pool and outputs the oracle gives.
+    b = _batch(63)
+    nd = sum(r.new_tokens for r in b.requests if r.kind == "decode")
+    assert all(r.kind == "decode" for r in b.requests[: b.num_decode])
+    st, st2 = torch.cuda.Stream(), torch.cuda.Stream()
+    dws = torch.empty(lib.decode_workspace_size(b.num_decode, 32, 8, 128), dtype=torch.uint8,
+                      device="cuda")
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+
+    def run(branches):
+        d = DeviceBatch(b)
+        d_out = torch.empty_like(d.dec_q)
+        d_lse = torch.empty(d.dec_q.shape[:2], dtype=torch.float32, device="cuda")
+        e_out = torch.empty_like(d.ext_q)
+        e_lse = torch.empty(d.ext_q.shape[:2], dtype=torch.float32, device="cuda")
+
+        def step():
+            s_ext = st2 if branches else st
+            if branches:
+                fork.record(st)
+                st2.wait_event(fork)
+            lib.kv_append(d.k_pool, d.v_pool, d.k_new[:nd], d.v_new[:nd], d.slot_mapping[:nd], stream=st)
+            lib.paged_decode(d.dec_q, d.k_pool, d.v_pool, d.dec_kv_indptr, d.dec_kv_indices,
+                             d.dec_kv_lens, b.sm_scale, out=d_out, lse=d_lse, workspace=dws, stream=st)
+            lib.kv_append(d.k_pool, d.v_pool, d.k_new[nd:], d.v_new[nd:], d.slot_mapping[nd:],
+                          stream=s_ext)
+            lib.paged_extend(d.ext_q, d.k_pool, d.v_pool, d.ext_qo_indptr, d.ext_kv_indptr,
+                             d.ext_kv_indices, d.ext_prefix_lens, b.max_extend_len, b.sm_scale,
+                             out=e_out, lse=e_lse, stream=s_ext)
+            if branches:
+                join.record(st2)
+                st.wait_event(join)
+
+        if branches:
+            with torch.cuda.stream(st):
+                step()  # warm-up outside the capture
+            st.synchronize()
+            d = DeviceBatch(b)  # fresh pool: the capture below must start from the same state
+            d_out.zero_(), d_lse.zero_(), e_out.zero_(), e_lse.zero_()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                step()
+            g.replay()
+        else:
+            with torch.cuda.stream(st):
+                step()
+        torch.cuda.synchronize()
+        return d, (d_out, d_lse, e_out, e_lse)
+
+    d_ser, serial = run(False)
+    d_br, branched = run(True)
+    for x, y in zip(branched, serial):
+        assert bits_equal(x, y) if x.dtype == torch.bfloat16 else torch.equal(x, y)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    assert bits_equal(d_br.k_pool, kp) and bits_equal(d_br.v_pool, vp)
+    o_ref, l_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices,
+                                       b.dec_kv_lens, 16, b.sm_scale)
+    assert_attention_close(branched[0], branched[1], o_ref, l_ref, what="two-branch decode")
+    o_ref, l_ref = oracle.paged_extend(b.ext_q, kp, vp, b.ext_qo_indptr, b.ext_kv_indptr,
+                                       b.ext_kv_indices, b.ext_prefix_lens, 16, b.sm_scale)
+    assert_attention_close(branched[2], branched[3], o_ref, l_ref, what="two-branch extend")
