@@ -467,7 +467,10 @@ def run_ours(args, ws, rank, local):
         "kernels": kernels,
         "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": (int(bool(app_ms)) + 2 * int(do_dec) + int(do_ext)) * K,
+        # kernels of the timed step: the append (two, one per branch, when the step is branched),
+        # decode and its split merge, extend
+        "gpu_launches": ((2 if overlap and not args.eager else int(bool(app_ms))) + 2 * int(do_dec)
+                         + int(do_ext)) * K,
         "clocks": clk,
     }
     return line
