@@ -25,6 +25,7 @@ import sys
 import tempfile
 import threading
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -68,6 +69,27 @@ def max_over_ranks(values, device=None):
 # ---------------------------------------------------------------------------------------------
 # algorithmic work of the workload (from the generated lengths)
 # ---------------------------------------------------------------------------------------------
+def _packed(named, device, pin=False):
+    """One byte buffer holding each (name, tensor) at a 256-byte-aligned offset, filled with the
+    tensors' values: returns (buffer, {name: view of the buffer})."""
+    import torch
+
+    offs, total = [], 0
+    for _, t in named:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = {}
+    for (name, t), off in zip(named, offs):
+        nb = t.numel() * t.element_size()
+        v = buf[off:off + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views[name] = v
+    return buf, views
+
+
 def workload_counts(b):
     import numpy as np
 
@@ -207,53 +229,84 @@ def run_ours(args, ws, rank, local):
     counts = workload_counts(b)
     st = torch.cuda.Stream(device=dev)
 
-    # device-resident state: the pool (the KV cache) and this step's inputs
+    # device-resident state: the pool (the KV cache).  A step's inputs and outputs each live in one
+    # buffer (256-byte-aligned views), so the end-to-end run moves them with one copy each way.
     kp, vp = b.k_pool.to(dev), b.v_pool.to(dev)
-    dq = b.dec_q.to(dev)
-    d_ind, d_idx, d_len = b.dec_kv_indptr.to(dev), b.dec_kv_indices.to(dev), b.dec_kv_lens.to(dev)
-    eq = b.ext_q.to(dev)
-    e_qo, e_ind, e_idx, e_pre = (b.ext_qo_indptr.to(dev), b.ext_kv_indptr.to(dev),
-                                 b.ext_kv_indices.to(dev), b.ext_prefix_lens.to(dev))
-    kn, vn, sm = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
+    inputs = [("kn", b.k_new), ("vn", b.v_new), ("sm", b.slot_mapping), ("d_ind", b.dec_kv_indptr),
+              ("d_idx", b.dec_kv_indices), ("d_len", b.dec_kv_lens), ("e_qo", b.ext_qo_indptr),
+              ("e_ind", b.ext_kv_indptr), ("e_idx", b.ext_kv_indices), ("e_pre", b.ext_prefix_lens)]
+    table = None
     if args.rope:
         # the step's queries are the new tokens' (decodes first, then extend tokens, the slot
         # order): one buffer the fused RoPE-append rotates in place, with decode/extend views
-        q_all = torch.cat([b.dec_q, b.ext_q]).to(dev)
-        dq, eq = q_all[: b.num_decode], q_all[b.num_decode:]
         pos = []
         for r in b.requests:
             pos += list(range(r.kv_len - r.new_tokens, r.kv_len))
-        positions = torch.tensor(pos, dtype=torch.int32, device=dev)
+        inputs += [("q_all", torch.cat([b.dec_q, b.ext_q])),
+                   ("positions", torch.tensor(pos, dtype=torch.int32))]
         table = pkv.rope_cos_sin_table(max(pos) + 1, b.head_dim, 1.0e6, device=dev)
-    d_out = torch.empty_like(dq)
-    d_lse = torch.empty((b.num_decode, b.num_q_heads), dtype=torch.float32, device=dev)
-    e_out = torch.empty_like(eq)
-    e_lse = torch.empty((eq.shape[0], b.num_q_heads), dtype=torch.float32, device=dev)
+    else:
+        inputs += [("dq", b.dec_q), ("eq", b.ext_q)]
     ws_bytes = pkv.decode_workspace_size(b.num_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, dev)
     dws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     max_e = b.max_extend_len
+
+    def make_bufs():
+        """One set of the step's device inputs and outputs (views of two packed buffers)."""
+        f = types.SimpleNamespace()
+        f.in_buf, din = _packed(inputs, dev)
+        for n in ("kn", "vn", "sm", "d_ind", "d_idx", "d_len", "e_qo", "e_ind", "e_idx", "e_pre"):
+            setattr(f, n, din[n])
+        if args.rope:
+            f.q_all, f.positions = din["q_all"], din["positions"]
+            f.dq, f.eq = f.q_all[: b.num_decode], f.q_all[b.num_decode:]
+        else:
+            f.q_all = f.positions = None
+            f.dq, f.eq = din["dq"], din["eq"]
+        outputs = [("d_out", torch.empty(f.dq.shape, dtype=f.dq.dtype)),
+                   ("d_lse", torch.empty((b.num_decode, b.num_q_heads), dtype=torch.float32)),
+                   ("e_out", torch.empty(f.eq.shape, dtype=f.eq.dtype)),
+                   ("e_lse", torch.empty((f.eq.shape[0], b.num_q_heads), dtype=torch.float32))]
+        f.out_buf, dout = _packed(outputs, dev)
+        f.d_out, f.d_lse, f.e_out, f.e_lse = dout["d_out"], dout["d_lse"], dout["e_out"], dout["e_lse"]
+        return f
+
+    bufs = make_bufs()
 
     do_app = args.op in ("all", "append")
     do_dec = args.op in ("all", "decode") and b.num_decode > 0
     do_ext = args.op in ("all", "extend") and b.num_extend > 0
 
-    def step(ev=None):
+    def append_range(f, lo, hi, stream):
+        if hi <= lo:
+            return
+        if args.rope:
+            pkv.rope_kv_append(kp, vp, f.kn[lo:hi], f.vn[lo:hi], f.sm[lo:hi], f.positions[lo:hi],
+                               table, q=f.q_all[lo:hi], stream=stream)
+        else:
+            pkv.kv_append(kp, vp, f.kn[lo:hi], f.vn[lo:hi], f.sm[lo:hi], stream=stream)
+
+    def decode(f, stream):
+        pkv.paged_decode(f.dq, kp, vp, f.d_ind, f.d_idx, f.d_len, b.sm_scale, out=f.d_out,
+                         lse=f.d_lse, workspace=dws, stream=stream)
+
+    def extend(f, stream):
+        pkv.paged_extend(f.eq, kp, vp, f.e_qo, f.e_ind, f.e_idx, f.e_pre, max_e, b.sm_scale,
+                         out=f.e_out, lse=f.e_lse, stream=stream)
+
+    def step(f=bufs, ev=None):
         if ev is not None:
             ev[0].record(st)
-        if do_app and args.rope:
-            pkv.rope_kv_append(kp, vp, kn, vn, sm, positions, table, q=q_all, stream=st)
-        elif do_app:
-            pkv.kv_append(kp, vp, kn, vn, sm, stream=st)
+        if do_app:
+            append_range(f, 0, f.kn.shape[0], st)
         if ev is not None:
             ev[1].record(st)
         if do_dec:
-            pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
-                             workspace=dws, stream=st)
+            decode(f, st)
         if ev is not None:
             ev[2].record(st)
         if do_ext:
-            pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
-                             lse=e_lse, stream=st)
+            extend(f, st)
         if ev is not None:
             ev[3].record(st)
 
@@ -268,24 +321,13 @@ def run_ours(args, ws, rank, local):
     st2 = torch.cuda.Stream(device=dev)
     fork_ev, join_ev = torch.cuda.Event(), torch.cuda.Event()
 
-    def append_range(lo, hi, stream):
-        if hi <= lo:
-            return
-        if args.rope:
-            pkv.rope_kv_append(kp, vp, kn[lo:hi], vn[lo:hi], sm[lo:hi], positions[lo:hi], table,
-                               q=q_all[lo:hi], stream=stream)
-        else:
-            pkv.kv_append(kp, vp, kn[lo:hi], vn[lo:hi], sm[lo:hi], stream=stream)
-
-    def step_branches():
+    def step_branches(f=bufs):
         fork_ev.record(st)
         st2.wait_event(fork_ev)
-        append_range(0, nd_new, st)
-        pkv.paged_decode(dq, kp, vp, d_ind, d_idx, d_len, b.sm_scale, out=d_out, lse=d_lse,
-                         workspace=dws, stream=st)
-        append_range(nd_new, kn.shape[0], st2)
-        pkv.paged_extend(eq, kp, vp, e_qo, e_ind, e_idx, e_pre, max_e, b.sm_scale, out=e_out,
-                         lse=e_lse, stream=st2)
+        append_range(f, 0, nd_new, st)
+        decode(f, st)
+        append_range(f, nd_new, f.kn.shape[0], st2)
+        extend(f, st2)
         join_ev.record(st2)
         st.wait_event(join_ev)
 
@@ -315,7 +357,7 @@ def run_ours(args, ws, rank, local):
         for k in range(K):
             if flush is not None:
                 flush.zero_()
-            step(evs[k])
+            step(ev=evs[k])
         stop.record(st)
     torch.cuda.synchronize(dev)
     barrier()
@@ -354,40 +396,51 @@ def run_ours(args, ws, rank, local):
     t_ext = [e[2].elapsed_time(e[3]) for e in evs]
 
     # ---- end to end through the public API with host buffers -----------------------------
-    host_in = {n: t.pin_memory() for n, t in (("dq", b.dec_q), ("eq", b.ext_q), ("kn", b.k_new),
-                                               ("vn", b.v_new), ("sm", b.slot_mapping),
-                                               ("d_ind", b.dec_kv_indptr), ("d_idx", b.dec_kv_indices),
-                                               ("d_len", b.dec_kv_lens), ("e_qo", b.ext_qo_indptr),
-                                               ("e_ind", b.ext_kv_indptr), ("e_idx", b.ext_kv_indices),
-                                               ("e_pre", b.ext_prefix_lens))}
-    dev_in = {"dq": dq, "eq": eq, "kn": kn, "vn": vn, "sm": sm, "d_ind": d_ind, "d_idx": d_idx,
-              "d_len": d_len, "e_qo": e_qo, "e_ind": e_ind, "e_idx": e_idx, "e_pre": e_pre}
-    host_out = {"d_out": torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory(),
-                "d_lse": torch.empty(d_lse.shape, dtype=d_lse.dtype).pin_memory(),
-                "e_out": torch.empty(e_out.shape, dtype=e_out.dtype).pin_memory(),
-                "e_lse": torch.empty(e_lse.shape, dtype=e_lse.dtype).pin_memory()}
-    dev_out = {"d_out": d_out, "d_lse": d_lse, "e_out": e_out, "e_lse": e_lse}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # Every step copies its inputs from pinned host memory (one buffer, laid out as on the
+    # device), runs, and copies all its outputs back.  Two device buffer sets let the copies of
+    # one step overlap the computation of its neighbours: the inputs of step k+1 go in and the
+    # outputs of step k-1 come out while step k computes, on their own copy streams.
+    host_in_buf, _ = _packed(inputs, "cpu", pin=True)
+    host_out_buf = torch.empty(bufs.out_buf.numel(), dtype=torch.uint8).pin_memory()
+    h2d = host_in_buf.numel()
+    d2h = host_out_buf.numel()
+    sets = [bufs, make_bufs()]
+    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        whole_step()
-        for n, t in host_out.items():
-            t.copy_(dev_out[n], non_blocking=True)
+    def e2e_step(k):
+        i = k % 2
+        f = sets[i]
+        if k >= 2:
+            cs_in.wait_event(ev_comp[i])  # step k-2 has finished reading set i's inputs
+        with torch.cuda.stream(cs_in):
+            f.in_buf.copy_(host_in_buf, non_blocking=True)
+        ev_in[i].record(cs_in)
+        st.wait_event(ev_in[i])
+        if k >= 2:
+            st.wait_event(ev_out[i])  # step k-2's outputs (set i) are back on the host
+        whole_step(f)
+        ev_comp[i].record(st)
+        cs_out.wait_event(ev_comp[i])
+        with torch.cuda.stream(cs_out):
+            host_out_buf.copy_(f.out_buf, non_blocking=True)
+        ev_out[i].record(cs_out)
 
     K2 = max(1, min(K, 200)) if not args.no_e2e else 1
     with torch.cuda.stream(st):
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for k in range(max(2, args.warmup)):
+            e2e_step(k)
     torch.cuda.synchronize(dev)
     barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(st):
         s2.record(st)
-        for _ in range(K2):
-            e2e_step()
+        cs_in.wait_event(s2)
+        for k in range(K2):
+            e2e_step(k)
+        st.wait_event(ev_out[(K2 - 1) % 2])  # the last step's outputs are on the host
         e2.record(st)
     torch.cuda.synchronize(dev)
     barrier()
@@ -461,6 +514,8 @@ def run_ours(args, ws, rank, local):
             + ("; two branches: (append of the decodes' tokens, decode, merge) beside (append of the "
                "extend tokens, extend)" if overlap else "; one stream")
             + " (per-kernel times from an eager pass on one stream)",
+        "e2e_copies": "each step's inputs (one pinned buffer) in and outputs out on two copy streams, "
+                      "overlapping the neighbouring steps' computation (two device buffer sets)",
         },
         "ms_per_step_eager": round(eager_ms / K, 4),
         "roofline": roofline,
