@@ -95,6 +95,8 @@ CASES = [
     (128, 16, 1, [(5, 130), (250, 10)]),
     (256, 16, 16, [(300, 100)]),
     (16, 32, 2, [(31, 17), (0, 9)]),
+    (32, 16, 8, [(0, 3), (50, 0), (999, 77)]),          # group 2; a request with no new token
+    (16, 32, 8, [(40, 0), (0, 1), (17, 0), (300, 64)]),  # empty extends between others
 ]
 
 
