@@ -25,6 +25,8 @@
 //    movmatrix.  KV is read exactly once per CTA per token, for all heads of the group.
 #include <float.h>
 
+#include <atomic>
+
 #include <mutex>
 #include <type_traits>
 
@@ -819,13 +821,20 @@ bool make_plan(int B, int Hq, int Hkv, int D, int ncta, DecodePlan& p, int page_
 template <int D, int NT, bool TMA>
 pkv_status launch_decode(const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
   auto kern = paged_decode_kernel<D, NT, TMA>;
-  static int configured_dev[64] = {0};
+  // the dynamic shared-memory limit this instance was raised to, per device (any host thread)
+  static std::atomic<int> configured_dev[64];
   const int dev = pkv_host::current_device();
-  if (dev >= 0 && dev < 64 && configured_dev[dev] < (int)p.smem) {
+  if (dev < 0) return PKV_ERR_CUDA;
+  if (dev >= 64 || configured_dev[dev].load(std::memory_order_relaxed) < (int)p.smem) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
-    configured_dev[dev] = (int)p.smem;
+    if (dev < 64) {
+      int cur = configured_dev[dev].load(std::memory_order_relaxed);
+      while (cur < (int)p.smem &&
+             !configured_dev[dev].compare_exchange_weak(cur, (int)p.smem, std::memory_order_relaxed)) {
+      }
+    }
   }
   const int threads = (p.HC * p.W + 1) * 32;
   kern<<<p.ncta, threads, p.smem, st>>>(a);

@@ -29,6 +29,8 @@
 //    row into a shared-memory tile that all eight warps copy out with coalesced stores.
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
+#include <atomic>
+
 #include "tc05.cuh"
 
 namespace {
@@ -558,14 +560,15 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
   a.tokens_per_tile = tpt;
   a.scale_log2 = sm_scale * kLog2e;
 
-  static bool configured[64] = {false};
+  // whether the kernel's dynamic shared-memory limit was raised on this device (any host thread)
+  static std::atomic<bool> configured[64];
   const int dev = pkv_host::current_device();
   if (dev < 0) return PKV_ERR_CUDA;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(paged_extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return PKV_ERR_CUDA;
-    if (dev < 64) configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_relaxed);
   }
   const int tiles = (max_extend_len + tpt - 1) / tpt;
   dim3 grid(tiles, pool->num_kv_heads, batch_size);
