@@ -118,12 +118,24 @@ def workload_counts(b):
         E = qo[r + 1] - qo[r]
         pairs += E * pref[r] + E * (E + 1) // 2
     ext_flops = 4 * D * Hq * pairs
+    # extend bytes: each physical KV slot of the extend requests once (prefix and new rows), K and
+    # V; the queries in, outputs and LSE out; the page lists
+    eptr = b.ext_kv_indptr.numpy()
+    eind = b.ext_kv_indices.numpy().astype(np.int64)
+    eslots = []
+    for r in range(len(pref)):
+        pos = np.arange(pref[r] + qo[r + 1] - qo[r])
+        eslots.append(eind[eptr[r] + pos // ps] * ps + pos % ps)
+    euniq = np.unique(np.concatenate(eslots)).size if len(eslots) else 0
+    ext_bytes = (euniq * row * 2 + int(qo[-1]) * Hq * (D * 2 * 2 + 4)
+                 + (eptr.size + eind.size + pref.size + qo.size) * 4)
     T = b.num_new_tokens
     app_bytes = T * row * 2 * 2 + T * 8  # read new K/V, write K/V rows, slots
     tokens = len(lens) + int(qo[-1])
     return {"decode_bytes": int(dec_bytes), "decode_bytes_logical": int(dec_bytes_logical),
             "decode_kv_tokens_unique": int(uniq), "decode_kv_tokens_logical": logical,
-            "extend_flops": int(ext_flops), "extend_pairs": int(pairs), "append_bytes": int(app_bytes),
+            "extend_flops": int(ext_flops), "extend_pairs": int(pairs), "extend_bytes": int(ext_bytes),
+            "append_bytes": int(app_bytes),
             "attn_tokens": int(tokens)}
 
 
@@ -249,6 +261,9 @@ def run_ours(args, ws, rank, local):
         inputs += [("dq", b.dec_q), ("eq", b.ext_q)]
     ws_bytes = pkv.decode_workspace_size(b.num_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, dev)
     dws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ext_ws = pkv.extend_workspace_size(b.num_extend, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                       b.max_extend_len, dev) if b.num_extend else 0
+    ews = torch.empty(max(256, ext_ws), dtype=torch.uint8, device=dev)
     max_e = b.max_extend_len
 
     def make_bufs():
@@ -292,7 +307,7 @@ def run_ours(args, ws, rank, local):
 
     def extend(f, stream):
         pkv.paged_extend(f.eq, kp, vp, f.e_qo, f.e_ind, f.e_idx, f.e_pre, max_e, b.sm_scale,
-                         out=f.e_out, lse=f.e_lse, stream=stream)
+                         out=f.e_out, lse=f.e_lse, workspace=ews, stream=stream)
 
     def step(f=bufs, ev=None):
         if ev is not None:
@@ -467,9 +482,12 @@ def run_ours(args, ws, rank, local):
     ext_peak = peaks["bf16_tflops"] if not do_dec else peaks["bf16_tflops_sustained"]
     if ext_ms:
         ext_tflops = counts["extend_flops"] / (ext_ms / 1e3) / 1e12
+        ext_gbs = counts["extend_bytes"] / (ext_ms / 1e3) / 1e9
         kernels["extend"] = {"ms": round(ext_ms, 4), "tflops": round(ext_tflops, 1),
                              "frac_bf16": round(ext_tflops / ext_peak, 4), "peak_tflops": ext_peak,
-                             "flops": counts["extend_flops"]}
+                             "flops": counts["extend_flops"], "gbs": round(ext_gbs, 1),
+                             "frac_hbm": round(ext_gbs / peaks["hbm_gbs"], 4),
+                             "bytes": counts["extend_bytes"]}
     if app_ms:
         kernels["kv_append"] = {"ms": round(app_ms, 4),
                                 "gbs": round(counts["append_bytes"] / (app_ms / 1e3) / 1e9, 1)}
@@ -480,11 +498,18 @@ def run_ours(args, ws, rank, local):
                     "frac": kernels["decode"]["frac_hbm"], "traffic": traffic,
                     "algorithmic_bytes": counts["decode_bytes"],
                     "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
-    else:
+    elif counts["extend_flops"] * peaks["hbm_gbs"] >= counts["extend_bytes"] * ext_peak * 1e3:
+        # arithmetic intensity at or above the ridge point: bounded by the tensor cores
         roofline = {"kernel": "paged_extend", "bound": "tensor", "achieved": kernels["extend"]["tflops"],
                     "peak": ext_peak, "unit": "TFLOP/s", "frac": kernels["extend"]["frac_bf16"],
                     "traffic": None, "algorithmic_flops": counts["extend_flops"],
                     "peak_source": "of measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peaks["source"] == "measured" else "of fallback"}
+    else:
+        # few queries per KV row (speculative verify): bounded by reading the KV pages
+        roofline = {"kernel": "paged_extend", "bound": "hbm", "achieved": kernels["extend"]["gbs"],
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kernels["extend"]["frac_hbm"],
+                    "traffic": None, "algorithmic_bytes": counts["extend_bytes"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -523,9 +548,9 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": round(tokens * K2 * ws / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         # kernels of the timed step: the append (two, one per branch, when the step is branched),
-        # decode and its split merge, extend
+        # decode and its split merge, the extend's request ordering and the extend
         "gpu_launches": ((2 if overlap and not args.eager else int(bool(app_ms))) + 2 * int(do_dec)
-                         + int(do_ext)) * K,
+                         + (1 + int(ext_ws > 0)) * int(do_ext)) * K,
         "clocks": clk,
     }
     return line

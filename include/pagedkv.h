@@ -171,7 +171,9 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool* pool, const void* q, int32_t
                                     void* stream);
 
 /*
- * Bytes of workspace pkv_paged_extend needs (0 when none is needed).
+ * Bytes of workspace pkv_paged_extend needs: the order in which its grid visits the requests
+ * (longest KV first), int32 per request, for batches of up to 4096 requests; 0 above that (batch
+ * order).
  */
 size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_extend_len);
@@ -188,7 +190,9 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
  *   max_extend_len  an upper bound of qo_indptr[b+1]-qo_indptr[b] over b (sizes the grid;
  *              rows beyond it are not computed)
  *   out        bf16 [num_q_tokens, num_q_heads, head_dim]; lse nullable fp32 [num_q_tokens, num_q_heads]
- *   workspace  at least pkv_extend_workspace_size(...) bytes (may be NULL when that is 0)
+ *   workspace  device, 16-byte aligned, at least pkv_extend_workspace_size(...) bytes, caller-owned
+ *              and not shared with a call in flight on another stream (may be NULL when that
+ *              size is 0); smaller returns PKV_ERR_WORKSPACE
  * head_dim 128, page_size a power of two >= 8; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
  */
 pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,

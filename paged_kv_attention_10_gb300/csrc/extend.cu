@@ -88,6 +88,7 @@ struct ExtendArgs {
   int32_t log2_group;
   int32_t tokens_per_tile;
   float scale_log2;
+  const int32_t* order;  // request of grid z-index z, longest KV first (nullable: batch order)
 };
 
 struct Work {
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   // later tiles of a request attend over more positions: launch them first
   w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
   w.h = blockIdx.y;
-  w.b = blockIdx.z;
+  w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
   w.qo0 = __ldg(a.qo_indptr + w.b);
   w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
   if (w.t0 >= w.E) return;  // uniform: this tile has no rows
@@ -487,6 +488,46 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   }
 }
 
+// Requests ordered by KV length (prefix + new tokens), longest first and ties by index, so that
+// the grid dispatches the CTAs with the most work first and the last wave holds short ones: a
+// bitonic sort of (length, index) keys in shared memory by one CTA.  n is a power of two >= B.
+constexpr int kMaxOrdered = 4096;
+
+__global__ void __launch_bounds__(1024) extend_order_kernel(const int32_t* __restrict__ qo_indptr,
+                                                            const int32_t* __restrict__ prefix_lens,
+                                                            int32_t B, int32_t n, int32_t* __restrict__ order) {
+  __shared__ unsigned long long key[kMaxOrdered];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    unsigned long long k = 0;  // padding sorts last
+    if (i < B) {
+      const int64_t L = (int64_t)max(0, __ldg(prefix_lens + i)) +
+                        max(0, __ldg(qo_indptr + i + 1) - __ldg(qo_indptr + i));
+      const unsigned long long len = (unsigned long long)min(L, (int64_t)0x7fffffff);
+      k = (len << 32) | (0xffffffffull - (unsigned)i);  // larger first; equal lengths by index
+    }
+    key[i] = k;
+  }
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = key[i], y = key[ixj];
+          const bool descending = (i & k) == 0;
+          if (descending ? x < y : x > y) {
+            key[i] = y;
+            key[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < B; i += blockDim.x)
+    order[i] = (int32_t)(0xffffffffull - (key[i] & 0xffffffffull));
+}
+
 // ---------------------------------------------------------------------------------------------
 // Host
 // ---------------------------------------------------------------------------------------------
@@ -503,12 +544,13 @@ extern "C" {
 
 size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_extend_len) {
-  (void)batch_size;
   (void)num_q_heads;
   (void)num_kv_heads;
   (void)head_dim;
   (void)max_extend_len;
-  return 0;
+  // the request order (int32 per request) when the batch is small enough to sort in one CTA
+  if (batch_size <= 0 || batch_size > kMaxOrdered) return 0;
+  return ((size_t)batch_size * 4 + 255) & ~(size_t)255;
 }
 
 pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
@@ -517,13 +559,15 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
                             const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             uint32_t* err_word, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || num_q_tokens < 0 ||
       max_extend_len < 0)
     return PKV_ERR_INVALID_ARG;
   if (batch_size == 0 || num_q_tokens == 0 || max_extend_len == 0) return PKV_OK;
   if (!q || !qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !out) return PKV_ERR_INVALID_ARG;
+  const size_t ws_need = pkv_extend_workspace_size(batch_size, num_q_heads, pool->num_kv_heads,
+                                                   pool->head_dim, max_extend_len);
+  if (ws_need > 0 && (!workspace || workspace_bytes < ws_need)) return PKV_ERR_WORKSPACE;
+  if (ws_need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
   if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (pool->head_dim != kHD) return PKV_ERR_UNSUPPORTED;
@@ -559,6 +603,16 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
   a.log2_group = lg;
   a.tokens_per_tile = tpt;
   a.scale_log2 = sm_scale * kLog2e;
+  a.order = nullptr;
+  if (ws_need > 0) {
+    int n = 1;
+    while (n < batch_size) n <<= 1;
+    extend_order_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(qo_indptr, prefix_lens, batch_size, n,
+                                                              (int32_t*)workspace);
+    const pkv_status st = pkv_host::launch_status();
+    if (st != PKV_OK) return st;
+    a.order = (const int32_t*)workspace;
+  }
 
   // whether the kernel's dynamic shared-memory limit was raised on this device (any host thread)
   static std::atomic<bool> configured[64];

@@ -97,6 +97,7 @@ CASES = [
     (16, 32, 2, [(31, 17), (0, 9)]),
     (32, 16, 8, [(0, 3), (50, 0), (999, 77)]),          # group 2; a request with no new token
     (16, 32, 8, [(40, 0), (0, 1), (17, 0), (300, 64)]),  # empty extends between others
+    (16, 32, 8, [((i * 37) % 300, (i * 11) % 40) for i in range(70)]),  # 70 requests, mixed lengths
 ]
 
 
@@ -168,6 +169,14 @@ def test_extend_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
     assert e.value.status == 2  # group size 3
+    b = random_small_batch(24, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                           extend=[(4, 4), (0, 9)])
+    need = lib.extend_workspace_size(2, 8, 2, 128, b.max_extend_len)
+    assert need > 0
+    with pytest.raises(lib.PagedKVError) as e:
+        run_extend(lib, b, b.k_pool, b.v_pool,
+                   workspace=torch.zeros(need - 16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 3  # workspace too small for the request order
 
 
 def test_extend_speculative_verify_shape(lib):

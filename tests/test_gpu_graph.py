@@ -30,13 +30,16 @@ def test_captured_step_matches_eager_and_oracle(lib):
     e_out = torch.empty_like(d.ext_q)
     e_lse = torch.empty(d.ext_q.shape[:2], dtype=torch.float32, device="cuda")
     max_e = max(b1.max_extend_len, b2.max_extend_len)
+    ews = torch.empty(max(256, lib.extend_workspace_size(b1.num_extend, 32, 8, 128, max_e)),
+                      dtype=torch.uint8, device="cuda")
 
     def step():
         lib.kv_append(d.k_pool, d.v_pool, d.k_new, d.v_new, d.slot_mapping, stream=st)
         lib.paged_decode(d.dec_q, d.k_pool, d.v_pool, d.dec_kv_indptr, d.dec_kv_indices, d.dec_kv_lens,
                          b1.sm_scale, out=d_out, lse=d_lse, workspace=dws, stream=st)
         lib.paged_extend(d.ext_q, d.k_pool, d.v_pool, d.ext_qo_indptr, d.ext_kv_indptr, d.ext_kv_indices,
-                         d.ext_prefix_lens, max_e, b1.sm_scale, out=e_out, lse=e_lse, stream=st)
+                         d.ext_prefix_lens, max_e, b1.sm_scale, out=e_out, lse=e_lse, workspace=ews,
+                         stream=st)
 
     with torch.cuda.stream(st):
         step()  # warm-up: one-time attribute setup happens outside the capture
@@ -83,6 +86,8 @@ def test_two_branch_step_matches_serial_and_oracle(lib):
     st, st2 = torch.cuda.Stream(), torch.cuda.Stream()
     dws = torch.empty(lib.decode_workspace_size(b.num_decode, 32, 8, 128), dtype=torch.uint8,
                       device="cuda")
+    ews = torch.empty(max(256, lib.extend_workspace_size(b.num_extend, 32, 8, 128, b.max_extend_len)),
+                      dtype=torch.uint8, device="cuda")
     fork, join = torch.cuda.Event(), torch.cuda.Event()
 
     def run(branches):
@@ -104,7 +109,7 @@ def test_two_branch_step_matches_serial_and_oracle(lib):
                           stream=s_ext)
             lib.paged_extend(d.ext_q, d.k_pool, d.v_pool, d.ext_qo_indptr, d.ext_kv_indptr,
                              d.ext_kv_indices, d.ext_prefix_lens, b.max_extend_len, b.sm_scale,
-                             out=e_out, lse=e_lse, stream=s_ext)
+                             out=e_out, lse=e_lse, workspace=ews, stream=s_ext)
             if branches:
                 join.record(st2)
                 st.wait_event(join)
