@@ -26,6 +26,7 @@ from .attention import (  # noqa: F401
     paged_extend,
     merge_states,
     decode_split_reference,
+    shared_prefix_attention,
     rope_angles,
     rope,
     rope_kv_append,

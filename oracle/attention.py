@@ -259,6 +259,45 @@ def paged_extend(q, k_pool, v_pool, qo_indptr, kv_indptr, kv_indices, prefix_len
     return o, lse
 
 
+def shared_prefix_attention(q, k_pool, v_pool, q_start, q_len, o_start, kv_indptr, kv_indices,
+                            kv_lens, num_out_rows, page_size, sm_scale):
+    """Attention of several requests' queries over KV pages they share (a cascade level).
+
+    Radix-cache prefix sharing (mini-sglang README, "KVcache Management") lets requests point at
+    the same physical pages for a common prefix.  Over those positions every sharer's query sees
+    every position (the prefix lies before all of its queries), so the part's state is plain
+    unmasked attention; merged with the state over the request's own pages (``merge_states``)
+    it gives the request's full attention.
+
+    Part p: query rows ``q_start[p] .. q_start[p] + q_len[p] - 1`` of q ``[Nq, Hq, D]``
+    attend to the ``kv_lens[p]`` positions of page list p (``kv_indptr``/``kv_indices``, as for
+    the decode), query head h reading KV head ``h // (Hq / Hkv)``.  Output row ``o_start[p] + i``
+    gets the normalised output and the natural-log LSE of query row ``q_start[p] + i``.  A part
+    with no positions gives ``o = 0``, ``lse = -inf``.  Returns ``(o [num_out_rows, Hq, D],
+    lse [num_out_rows, Hq])`` in fp64; rows that no part writes are NaN.
+    """
+    qf = as_f64(q)
+    _, Hq, D = qf.shape
+    Hkv = k_pool.shape[2]
+    qs, ql, os_ = _as_int(q_start), _as_int(q_len), _as_int(o_start)
+    lens = _as_int(kv_lens)
+    o = np.full((num_out_rows, Hq, D), np.nan)
+    lse = np.full((num_out_rows, Hq), np.nan)
+    for p in range(len(lens)):
+        L = int(lens[p])
+        n = int(ql[p])
+        Kp = as_f64(request_kv(k_pool, kv_indptr, kv_indices, p, L, page_size))
+        Vp = as_f64(request_kv(v_pool, kv_indptr, kv_indices, p, L, page_size))
+        rows_in = slice(int(qs[p]), int(qs[p]) + n)
+        rows_out = slice(int(os_[p]), int(os_[p]) + n)
+        for h in range(Hq):
+            g = _kv_head_of(h, Hq, Hkv)
+            res = attend_rows(qf[rows_in, h], Kp[:, g], Vp[:, g], np.full(n, L), sm_scale)
+            o[rows_out, h] = res[0]
+            lse[rows_out, h] = res[1]
+    return o, lse
+
+
 def decode_split_reference(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, page_size, sm_scale, bounds):
     """Decode computed as split partials over ``bounds`` and merged.
 
