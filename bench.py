@@ -139,6 +139,28 @@ def workload_counts(b):
             "attn_tokens": int(tokens)}
 
 
+def cascade_counts(b, plan):
+    """Algorithmic work of the cascade's pieces: the shared-prefix parts' unmasked (query, key)
+    flops, the own-pages decode's bytes (each physical slot once, plus q in, partial out) and the
+    merge's bytes (every partial state read, the output written)."""
+    import numpy as np
+
+    Hkv, D, Hq, ps = b.num_kv_heads, b.head_dim, b.num_q_heads, b.page_size
+    row = Hkv * D * 2
+    ql = plan.part_q_len.numpy().astype(np.int64)
+    kl = plan.part_kv_lens.numpy().astype(np.int64)
+    prefix_flops = int(4 * D * Hq * (ql * kl).sum())
+    ind = plan.suffix_kv_indices.numpy().astype(np.int64)
+    ptr = plan.suffix_kv_indptr.numpy()
+    lens = plan.suffix_kv_lens.numpy().astype(np.int64)
+    slots = [ind[ptr[r] + np.arange(lens[r]) // ps] * ps + np.arange(lens[r]) % ps for r in range(len(lens))]
+    uniq = np.unique(np.concatenate(slots)).size if slots else 0
+    B = len(lens)
+    suffix_bytes = uniq * row * 2 + B * Hq * (D * 2 * 2 + 4) + (ptr.size + ind.size + lens.size) * 4
+    merge_bytes = (plan.num_splits + 1) * B * Hq * (D * 2 + 4) + B * Hq * (D * 2 + 4)
+    return {"prefix_flops": prefix_flops, "suffix_bytes": int(suffix_bytes), "merge_bytes": int(merge_bytes)}
+
+
 # ---------------------------------------------------------------------------------------------
 # clocks sampled by nvidia-smi during the timed region
 # ---------------------------------------------------------------------------------------------
@@ -259,6 +281,36 @@ def run_ours(args, ws, rank, local):
         table = pkv.rope_cos_sin_table(max(pos) + 1, b.head_dim, 1.0e6, device=dev)
     else:
         inputs += [("dq", b.dec_q), ("eq", b.ext_q)]
+    plan = None
+    if args.cascade:
+        from paged_kv_attention_10_gb300.cascade import plan_shared_prefix
+
+        # each share group must be a run of consecutive decode requests
+        groups = {}
+        for i, r in enumerate(b.requests[: b.num_decode]):
+            if r.share_group >= 0:
+                groups.setdefault(r.share_group, []).append(i)
+        for g, rows in groups.items():
+            if rows != list(range(rows[0], rows[0] + len(rows))):
+                raise SystemExit(f"--cascade: share group {g} is not a run of consecutive requests")
+        plan = plan_shared_prefix(b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
+                                  [(rows[0], len(rows)) for rows in groups.values()], b.page_size,
+                                  num_kv_heads=b.num_kv_heads, group_size=b.num_q_heads // b.num_kv_heads,
+                                  num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+        # the step's metadata is the plan's: the parts, and each request's own pages
+        inputs = [x for x in inputs if x[0] not in ("d_ind", "d_idx", "d_len")]
+        inputs += [("d_ind", plan.suffix_kv_indptr), ("d_idx", plan.suffix_kv_indices),
+                   ("d_len", plan.suffix_kv_lens), ("p_qs", plan.part_q_start), ("p_ql", plan.part_q_len),
+                   ("p_os", plan.part_o_start), ("p_ind", plan.part_kv_indptr),
+                   ("p_idx", plan.part_kv_indices), ("p_len", plan.part_kv_lens)]
+        S = plan.num_splits
+        o_parts = torch.empty((S + 1, b.num_decode, b.num_q_heads, b.head_dim), dtype=torch.bfloat16,
+                              device=dev)
+        lse_parts = torch.empty((S + 1, b.num_decode, b.num_q_heads), dtype=torch.float32, device=dev)
+        pws = torch.empty(max(256, pkv.shared_prefix_workspace_size(plan.num_parts, b.num_q_heads,
+                                                                    b.num_kv_heads, b.head_dim,
+                                                                    plan.max_part_rows, dev)),
+                          dtype=torch.uint8, device=dev)
     ws_bytes = pkv.decode_workspace_size(b.num_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, dev)
     dws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ext_ws = pkv.extend_workspace_size(b.num_extend, b.num_q_heads, b.num_kv_heads, b.head_dim,
@@ -272,6 +324,9 @@ def run_ours(args, ws, rank, local):
         f.in_buf, din = _packed(inputs, dev)
         for n in ("kn", "vn", "sm", "d_ind", "d_idx", "d_len", "e_qo", "e_ind", "e_idx", "e_pre"):
             setattr(f, n, din[n])
+        if plan is not None:
+            for n in ("p_qs", "p_ql", "p_os", "p_ind", "p_idx", "p_len"):
+                setattr(f, n, din[n])
         if args.rope:
             f.q_all, f.positions = din["q_all"], din["positions"]
             f.dq, f.eq = f.q_all[: b.num_decode], f.q_all[b.num_decode:]
@@ -301,9 +356,24 @@ def run_ours(args, ws, rank, local):
         else:
             pkv.kv_append(kp, vp, f.kn[lo:hi], f.vn[lo:hi], f.sm[lo:hi], stream=stream)
 
-    def decode(f, stream):
-        pkv.paged_decode(f.dq, kp, vp, f.d_ind, f.d_idx, f.d_len, b.sm_scale, out=f.d_out,
-                         lse=f.d_lse, workspace=dws, stream=stream)
+    def decode(f, stream, sub=None):
+        if plan is None:
+            pkv.paged_decode(f.dq, kp, vp, f.d_ind, f.d_idx, f.d_len, b.sm_scale, out=f.d_out,
+                             lse=f.d_lse, workspace=dws, stream=stream, max_ctas=decode_ctas)
+            return
+        # shared pages once per group (splits 0..S-1), each request's own pages (split S), merge
+        # (the scratch partial states are shared by both buffer sets: steps run in stream order)
+        H, D = b.num_q_heads, b.head_dim
+        pkv.shared_prefix_attention(f.dq, kp, vp, f.p_qs, f.p_ql, f.p_os, f.p_ind, f.p_idx, f.p_len,
+                                    plan.max_part_rows, b.sm_scale, o_parts.view(-1, H, D),
+                                    lse_parts.view(-1, H), workspace=pws, stream=stream)
+        if sub is not None:
+            sub[0].record(stream)
+        pkv.paged_decode(f.dq, kp, vp, f.d_ind, f.d_idx, f.d_len, b.sm_scale, out=o_parts[S],
+                         lse=lse_parts[S], workspace=dws, stream=stream, max_ctas=decode_ctas)
+        if sub is not None:
+            sub[1].record(stream)
+        pkv.merge_states(o_parts, lse_parts, out=f.d_out, lse=f.d_lse, stream=stream)
 
     def extend(f, stream):
         pkv.paged_extend(f.eq, kp, vp, f.e_qo, f.e_ind, f.e_idx, f.e_pre, max_e, b.sm_scale,
@@ -317,7 +387,7 @@ def run_ours(args, ws, rank, local):
         if ev is not None:
             ev[1].record(st)
         if do_dec:
-            decode(f, st)
+            decode(f, st, sub=ev[4:6] if ev is not None and len(ev) > 4 else None)
         if ev is not None:
             ev[2].record(st)
         if do_ext:
@@ -335,6 +405,13 @@ def run_ours(args, ws, rank, local):
                and (not args.rope or nd_new == b.num_decode))
     st2 = torch.cuda.Stream(device=dev)
     fork_ev, join_ev = torch.cuda.Event(), torch.cuda.Event()
+    # SMs the decode runs on: in the branched step a few stay free for the extend beside it (the
+    # decode is HBM-bound, the extend tensor-bound); otherwise all of them
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if args.decode_sms >= 0:
+        decode_ctas = args.decode_sms
+    else:
+        decode_ctas = sms - 16 if overlap and not args.eager else 0
 
     def step_branches(f=bufs):
         fork_ev.record(st)
@@ -359,7 +436,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- device-resident timed region ----------------------------------------------------
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4 if plan is None else 6)] for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier()
@@ -472,11 +549,33 @@ def run_ours(args, ws, rank, local):
     ext_ms = statistics.mean(t_ext) if do_ext else None
     app_ms = statistics.mean(t_app) if (do_app and b.num_new_tokens) else None
     kernels = {}
+    # decode and its split merge; with the cascade also the part order, the shared-prefix kernel and
+    # the final merge
+    dec_launches = 2 if plan is None else 4 + int(
+        pkv.shared_prefix_workspace_size(plan.num_parts, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                         plan.max_part_rows, dev) > 0)
     if dec_ms:
         dec_gbs = counts["decode_bytes"] / (dec_ms / 1e3) / 1e9
         kernels["decode"] = {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
                              "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
                              "gbs_logical": round(counts["decode_bytes_logical"] / (dec_ms / 1e3) / 1e9, 1)}
+    if dec_ms and plan is not None:
+        # the cascade's pieces: the whole path above counts every unique KV byte once
+        cc = cascade_counts(b, plan)
+        t_pre = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
+        t_suf = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
+        t_mrg = statistics.mean(e[5].elapsed_time(e[2]) for e in evs)
+        pre_tf = cc["prefix_flops"] / (t_pre / 1e3) / 1e12
+        suf_gbs = cc["suffix_bytes"] / (t_suf / 1e3) / 1e9
+        kernels["decode"]["path"] = "cascade: shared-prefix parts + own-pages decode + merge"
+        kernels["shared_prefix"] = {"ms": round(t_pre, 4), "tflops": round(pre_tf, 1),
+                                    "frac_bf16": round(pre_tf / peaks["bf16_tflops_sustained"], 4),
+                                    "peak_tflops": peaks["bf16_tflops_sustained"], "flops": cc["prefix_flops"]}
+        kernels["own_pages_decode"] = {"ms": round(t_suf, 4), "gbs": round(suf_gbs, 1),
+                                       "frac_hbm": round(suf_gbs / peaks["hbm_gbs"], 4),
+                                       "bytes": cc["suffix_bytes"]}
+        kernels["merge"] = {"ms": round(t_mrg, 4),
+                            "gbs": round(cc["merge_bytes"] / (t_mrg / 1e3) / 1e9, 1)}
     # the extend runs alone in its step on the radix-extend workload (burst peak), inside a long
     # step otherwise (sustained peak)
     ext_peak = peaks["bf16_tflops"] if not do_dec else peaks["bf16_tflops_sustained"]
@@ -492,7 +591,20 @@ def run_ours(args, ws, rank, local):
         kernels["kv_append"] = {"ms": round(app_ms, 4),
                                 "gbs": round(counts["append_bytes"] / (app_ms / 1e3) / 1e9, 1)}
     traffic = _traffic_record() if args.workload == "mixed" else None
-    if dec_ms:
+    if dec_ms and plan is not None and kernels["own_pages_decode"]["ms"] >= kernels["shared_prefix"]["ms"]:
+        k = kernels["own_pages_decode"]
+        roofline = {"kernel": "paged_decode over each request's own pages (decode + split merge)",
+                    "bound": "hbm", "achieved": k["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": k["frac_hbm"], "traffic": None, "algorithmic_bytes": k["bytes"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
+    elif dec_ms and plan is not None:
+        k = kernels["shared_prefix"]
+        roofline = {"kernel": "shared-prefix attention (paged_extend_kernel, unmasked parts)",
+                    "bound": "tensor", "achieved": k["tflops"], "peak": k["peak_tflops"],
+                    "unit": "TFLOP/s", "frac": k["frac_bf16"], "traffic": None,
+                    "algorithmic_flops": k["flops"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json bf16_tflops_sustained)" if peaks["source"] == "measured" else "of fallback"}
+    elif dec_ms:
         roofline = {"kernel": "paged_decode (decode + split merge)", "bound": "hbm",
                     "achieved": kernels["decode"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": kernels["decode"]["frac_hbm"], "traffic": traffic,
@@ -535,6 +647,11 @@ def run_ours(args, ws, rank, local):
                    "inputs larger than L2: each step reads ~%.1f GB of KV" % (counts["decode_bytes_logical"] / 1e9)),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "append": "fused RoPE (theta 1e6) + KV append, queries rotated in place" if args.rope else "KV append",
+            "decode_path": ("plain paged decode" if plan is None else
+                            f"shared-prefix cascade: {plan.num_parts} parts in {plan.num_splits} splits of "
+                            f"the shared pages ({plan.shared_tokens} tokens) on tensor cores, a decode over "
+                            "each request's own pages, bf16 partial-state merge"),
+            "decode_sms": decode_ctas or sms,
             "launch": ("eager launches" if args.eager else "CUDA graph of the whole step")
             + ("; two branches: (append of the decodes' tokens, decode, merge) beside (append of the "
                "extend tokens, extend)" if overlap else "; one stream")
@@ -549,7 +666,7 @@ def run_ours(args, ws, rank, local):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         # kernels of the timed step: the append (two, one per branch, when the step is branched),
         # decode and its split merge, the extend's request ordering and the extend
-        "gpu_launches": ((2 if overlap and not args.eager else int(bool(app_ms))) + 2 * int(do_dec)
+        "gpu_launches": ((2 if overlap and not args.eager else int(bool(app_ms))) + dec_launches * int(do_dec)
                          + (1 + int(ext_ws > 0)) * int(do_ext)) * K,
         "clocks": clk,
     }
@@ -661,6 +778,10 @@ def load_workload(name):
         from workloads import make_spec_verify
 
         return make_spec_verify()
+    if name == "shared-prefix-decode":
+        from workloads import make_shared_prefix_decode
+
+        return make_shared_prefix_decode()
     if name == "profile":
         from workloads import random_small_batch
 
@@ -672,7 +793,11 @@ def load_workload(name):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="mixed", choices=sorted(WORKLOADS) + ["spec-verify", "profile"])
+    ap.add_argument("--workload", default="mixed",
+                    choices=sorted(WORKLOADS) + ["spec-verify", "shared-prefix-decode", "profile"])
+    ap.add_argument("--cascade", action="store_true",
+                    help="decode through the shared-prefix (cascade) plan: the shared pages once per "
+                         "group on tensor cores, each request's own pages, and a merge")
     ap.add_argument("--flush-l2", action="store_true",
                     help="zero a 256 MB buffer before every timed step (for workloads that fit in L2); "
                          "the step time is then the sum of the per-operation event times")
@@ -682,6 +807,9 @@ def main():
                     help="fuse the rotary embedding of the new K and of all queries into the append")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of the step captured as one CUDA graph")
+    ap.add_argument("--decode-sms", type=int, default=-1,
+                    help="SMs the decode may use (0 = all; default: all but 16 when the step's extend "
+                         "runs beside the decode in its own graph branch, else all)")
     ap.add_argument("--serial-step", action="store_true",
                     help="run the step's operations one after another on one stream (no branches)")
     ap.add_argument("--gpus", type=int, default=1)

@@ -59,6 +59,7 @@ typedef enum {
 #define PKV_DEVERR_LENGTH 0x4u   /* a KV length exceeds the request's pages, or a decode length is 0 */
 #define PKV_DEVERR_TIMEOUT 0x8u  /* a bounded in-kernel wait gave up */
 #define PKV_DEVERR_INTERNAL 0x10u /* a launch-time invariant failed and the CTA skipped its work */
+#define PKV_DEVERR_ROW_OOB 0x20u   /* a query or output row range outside q / out was skipped */
 
 typedef struct {
   void* k;              /* bf16 [num_pages, page_size, num_kv_heads, head_dim], 16-byte aligned */
@@ -147,6 +148,21 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
                             uint32_t* err_word, void* stream);
 
 /*
+ * pkv_paged_decode on at most max_ctas SMs: one persistent CTA per SM as always, but only
+ * max_ctas of them (0, or a value at or above the SM count, means every SM; negative is
+ * PKV_ERR_INVALID_ARG).  The other SMs stay free for kernels on other streams.  The decode is
+ * bound by HBM bandwidth, which a few SMs fewer still nearly saturate, so a tensor-core kernel
+ * running beside it (the step's extend, on its own stream) gains those SMs for little decode
+ * time.  Same arguments, workspace size, results and errors as pkv_paged_decode, whose call is
+ * this one with max_ctas = 0.
+ */
+pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                 int32_t num_q_heads, const int32_t* kv_indptr,
+                                 const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 uint32_t* err_word, int32_t max_ctas, void* stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  No counterpart on the pages: this is a
  * convenience of this library.  A serving engine that reserves a fixed share of HBM for its KV
  * pool, or code that must not call cudaMalloc (and take its implicit device synchronisation) in
@@ -203,6 +219,44 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
                             uint32_t* err_word, void* stream);
 
 /*
+ * Bytes of workspace pkv_shared_prefix_attention needs (the order of its parts, as for the extend).
+ */
+size_t pkv_shared_prefix_workspace_size(int32_t num_parts, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t max_part_rows);
+
+/*
+ * Shared-prefix (cascade) attention.  When several requests share the first pages of their KV
+ * (radix-cache prefix sharing: mini-sglang README, "KVcache Management"), the attention of all
+ * their queries over those pages is computed together, so each shared page is read once per
+ * part instead of once per request, and on tensor cores.  The result is a partial state of each
+ * query over the shared positions, merged with the partial state over the request's own pages
+ * (a decode over the suffix page list) by pkv_merge_states_bf16; split the shared pages over
+ * several parts to spread long prefixes over the GPU.
+ * Part p: query rows q_start[p] .. q_start[p] + q_len[p] - 1 of q attend, without a mask, to all
+ * kv_lens[p] positions of page list p (kv_indptr / kv_indices as for the decode), with GQA as in
+ * the extend; the part's output rows are o_start[p] .. o_start[p] + q_len[p] - 1 of o_part:
+ *   o_part[r, h, :] = sum_j softmax_j(scale * q . k_j) v_j,  lse_part[r, h] = ln sum_j exp(scale * q . k_j)
+ * A part with kv_lens[p] == 0 writes o = 0 and lse = -inf (an empty split for the merge).
+ *   q          bf16 [num_q_rows, num_q_heads, 128] (device)
+ *   q_start, q_len, o_start, kv_lens  int32 [num_parts]; kv_indptr int32 [num_parts+1] (device)
+ *   max_part_rows  an upper bound of q_len[p] (sizes the grid; rows beyond it are not computed)
+ *   o_part     bf16 [num_out_rows, num_q_heads, 128]; lse_part nullable fp32 [num_out_rows, num_q_heads]
+ *   workspace  as for pkv_paged_extend, pkv_shared_prefix_workspace_size(...) bytes
+ *   err_word   nullable; PKV_DEVERR_ROW_OOB for a part whose rows fall outside q or o_part (the part
+ *              is skipped), PKV_DEVERR_PAGE_OOB / PKV_DEVERR_LENGTH as for the extend
+ * head_dim 128, page_size a power of two >= 8, group size in {1, 2, 4, 8, 16}.  Parts that write
+ * the same output rows race; different parts may read the same query rows.
+ */
+pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int32_t num_q_rows,
+                                       const int32_t* q_start, const int32_t* q_len,
+                                       const int32_t* o_start, int32_t num_parts, int32_t num_q_heads,
+                                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                                       const int32_t* kv_lens, int32_t max_part_rows, float sm_scale,
+                                       void* o_part, float* lse_part, int32_t num_out_rows,
+                                       void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                                       void* stream);
+
+/*
  * Log-sum-exp merge of split partial states (flash-decoding).  For each row n and head h:
  *   lse[n,h] = ln sum_s exp(lse_parts[s,n,h]);  out[n,h,:] = sum_s exp(lse_parts[s,n,h] - lse[n,h]) * o_parts[s,n,h,:]
  * A split with lse_parts = -inf is empty and contributes nothing; if all are empty the row gets
@@ -216,6 +270,15 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
 pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
                             int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
                             float* lse, void* stream);
+
+/*
+ * pkv_merge_states with bf16 partial outputs, o_parts bf16 [num_splits, num_rows, num_heads,
+ * head_dim] (16-byte aligned), e.g. the shared-prefix parts and a decode over each request's own
+ * pages written into consecutive splits.  Accumulates in fp32.
+ */
+pkv_status pkv_merge_states_bf16(const void* o_parts, const float* lse_parts, int32_t num_splits,
+                                 int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                                 float* lse, void* stream);
 
 #ifdef __cplusplus
 }

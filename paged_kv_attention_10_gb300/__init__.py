@@ -20,9 +20,9 @@ import torch
 __all__ = [
     "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
     "paged_decode", "paged_decode_noalloc", "extend_workspace_size", "paged_extend",
-    "merge_states", "status_string",
-    "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB",
-    "DEVERR_LENGTH", "DEVERR_TIMEOUT", "DEVERR_INTERNAL",
+    "merge_states", "shared_prefix_workspace_size", "shared_prefix_attention", "cascade_decode",
+    "status_string", "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB",
+    "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT", "DEVERR_INTERNAL", "DEVERR_ROW_OOB",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +34,7 @@ DEVERR_SLOT_OOB = 0x2
 DEVERR_LENGTH = 0x4
 DEVERR_TIMEOUT = 0x8
 DEVERR_INTERNAL = 0x10
+DEVERR_ROW_OOB = 0x20
 
 _c_i32, _c_i64, _c_f32, _c_sz, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 
@@ -70,10 +71,17 @@ def load():
         "pkv_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32]),
         "pkv_paged_decode": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp, _vp,
                                       _c_sz, _vp, _vp]),
+        "pkv_paged_decode_ctas": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
+                                           _vp, _c_sz, _vp, _c_i32, _vp]),
         "pkv_extend_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
         "pkv_paged_extend": (_c_i32, [P, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_i32,
                                       _c_f32, _vp, _vp, _vp, _c_sz, _vp, _vp]),
         "pkv_merge_states": (_c_i32, [_vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp]),
+        "pkv_merge_states_bf16": (_c_i32, [_vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp]),
+        "pkv_shared_prefix_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
+        "pkv_shared_prefix_attention": (_c_i32, [P, _vp, _c_i32, _vp, _vp, _vp, _c_i32, _c_i32, _vp, _vp,
+                                                 _vp, _c_i32, _c_f32, _vp, _vp, _c_i32, _vp, _c_sz, _vp,
+                                                 _vp]),
         "pkv_rope_kv_append": (_c_i32, [P, _vp, _vp, _vp, _vp, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp]),
         "pkv_paged_decode_noalloc": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
                                               _vp, _vp]),
@@ -219,8 +227,9 @@ def decode_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim, devic
 
 
 def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: float, out=None,
-                 lse=None, workspace=None, err_word=None, stream=None, return_lse=True):
-    """Decode attention of q [B, Hq, D] over each request's paged KV. Returns (out, lse)."""
+                 lse=None, workspace=None, err_word=None, stream=None, return_lse=True, max_ctas=0):
+    """Decode attention of q [B, Hq, D] over each request's paged KV. Returns (out, lse).
+    ``max_ctas`` > 0 runs it on at most that many SMs (the rest stay free for other streams)."""
     pool = _pool(k_pool, v_pool)
     dev = k_pool.device
     _need(q, "q", torch.bfloat16, dev)
@@ -241,9 +250,15 @@ def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: fl
         if workspace is None:
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
-        _call("pkv_paged_decode", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
-              _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
-              _ptr(workspace), workspace.numel(), _ptr(err_word), _stream_ptr(stream, dev))
+        if max_ctas:
+            _call("pkv_paged_decode_ctas", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
+                  _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
+                  _ptr(workspace), workspace.numel(), _ptr(err_word), int(max_ctas),
+                  _stream_ptr(stream, dev))
+        else:
+            _call("pkv_paged_decode", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
+                  _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
+                  _ptr(workspace), workspace.numel(), _ptr(err_word), _stream_ptr(stream, dev))
     return out, lse
 
 
@@ -315,9 +330,11 @@ def paged_extend(q, k_pool, v_pool, qo_indptr, kv_indptr, kv_indices, prefix_len
 
 
 def merge_states(o_parts, lse_parts, out=None, lse=None, stream=None):
-    """LSE merge of split partials o_parts [S, N, H, D] fp32, lse_parts [S, N, H] fp32."""
+    """LSE merge of split partials o_parts [S, N, H, D] (fp32 or bf16), lse_parts [S, N, H] fp32."""
     dev = o_parts.device
-    _need(o_parts, "o_parts", torch.float32)
+    bf16 = o_parts.dtype == torch.bfloat16
+    fn = "pkv_merge_states_bf16" if bf16 else "pkv_merge_states"
+    _need(o_parts, "o_parts", torch.bfloat16 if bf16 else torch.float32)
     _need(lse_parts, "lse_parts", torch.float32, dev)
     S, N, H, D = o_parts.shape
     if lse_parts.shape != (S, N, H):
@@ -329,6 +346,75 @@ def merge_states(o_parts, lse_parts, out=None, lse=None, stream=None):
     _need(out, "out", torch.bfloat16, dev)
     _need(lse, "lse", torch.float32, dev)
     with torch.cuda.device(dev):
-        _call("pkv_merge_states", _ptr(o_parts), _ptr(lse_parts), S, N, H, D, _ptr(out), _ptr(lse),
+        _call(fn, _ptr(o_parts), _ptr(lse_parts), S, N, H, D, _ptr(out), _ptr(lse),
               _stream_ptr(stream, dev))
     return out, lse
+
+
+def shared_prefix_workspace_size(num_parts, num_q_heads, num_kv_heads, head_dim, max_part_rows,
+                                 device=None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(load().pkv_shared_prefix_workspace_size(num_parts, num_q_heads, num_kv_heads,
+                                                           head_dim, max_part_rows))
+
+
+def shared_prefix_attention(q, k_pool, v_pool, q_start, q_len, o_start, kv_indptr, kv_indices,
+                            kv_lens, max_part_rows: int, sm_scale: float, o_part, lse_part=None,
+                            workspace=None, err_word=None, stream=None):
+    """Unmasked attention of each part's query rows over the part's (shared) pages: the partial
+    states of a cascade level, written at rows o_start[p].. of o_part (bf16) and lse_part."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _need(q, "q", torch.bfloat16, dev)
+    for t, n in ((q_start, "q_start"), (q_len, "q_len"), (o_start, "o_start"), (kv_indptr, "kv_indptr"),
+                 (kv_indices, "kv_indices"), (kv_lens, "kv_lens")):
+        _need(t, n, torch.int32, dev)
+    _need(o_part, "o_part", torch.bfloat16, dev)
+    Nq, Hq, D = q.shape
+    if o_part.dim() != 3 or o_part.shape[1:] != q.shape[1:]:
+        raise ValueError("o_part must be [num_out_rows, num_q_heads, head_dim]")
+    n_out = o_part.shape[0]
+    if lse_part is not None:
+        _need(lse_part, "lse_part", torch.float32, dev)
+        if lse_part.shape != (n_out, Hq):
+            raise ValueError("lse_part must be [num_out_rows, num_q_heads]")
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, dev)
+    P = kv_lens.numel()
+    with torch.cuda.device(dev):
+        need = int(load().pkv_shared_prefix_workspace_size(P, Hq, pool.num_kv_heads, D, max_part_rows))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", torch.uint8, dev)
+        _call("pkv_shared_prefix_attention", ctypes.byref(pool), _ptr(q), Nq, _ptr(q_start), _ptr(q_len),
+              _ptr(o_start), P, Hq, _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_lens), int(max_part_rows),
+              float(sm_scale), _ptr(o_part), _ptr(lse_part), n_out, _ptr(workspace),
+              0 if workspace is None else workspace.numel(), _ptr(err_word), _stream_ptr(stream, dev))
+    return o_part, lse_part
+
+
+def cascade_decode(q, k_pool, v_pool, plan, sm_scale: float, out=None, lse=None, o_parts=None,
+                   lse_parts=None, prefix_workspace=None, decode_workspace=None, err_word=None,
+                   stream=None):
+    """Decode through a shared-prefix plan (``cascade.plan_shared_prefix``, its tensors on the
+    device): the shared-prefix states, the decode over each request's own pages into the last
+    split, and their log-sum-exp merge.  Three library calls on one stream; returns (out, lse)."""
+    dev = q.device
+    B, Hq, D = q.shape
+    S = plan.num_splits
+    if o_parts is None:
+        o_parts = torch.empty((S + 1, B, Hq, D), dtype=torch.bfloat16, device=dev)
+    if lse_parts is None:
+        lse_parts = torch.empty((S + 1, B, Hq), dtype=torch.float32, device=dev)
+    if o_parts.shape != (S + 1, B, Hq, D) or lse_parts.shape != (S + 1, B, Hq):
+        raise ValueError("o_parts / lse_parts must be [num_splits + 1, B, Hq, (D)]")
+    shared_prefix_attention(q, k_pool, v_pool, plan.part_q_start, plan.part_q_len, plan.part_o_start,
+                            plan.part_kv_indptr, plan.part_kv_indices, plan.part_kv_lens,
+                            plan.max_part_rows, sm_scale, o_parts.view(-1, Hq, D),
+                            lse_parts.view(-1, Hq), workspace=prefix_workspace, err_word=err_word,
+                            stream=stream)
+    paged_decode(q, k_pool, v_pool, plan.suffix_kv_indptr, plan.suffix_kv_indices, plan.suffix_kv_lens,
+                 sm_scale, out=o_parts[S], lse=lse_parts[S], workspace=decode_workspace,
+                 err_word=err_word, stream=stream)
+    return merge_states(o_parts, lse_parts, out=out, lse=lse, stream=stream)

@@ -624,14 +624,17 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const __grid_const
   fence_proxy_async_smem();
   __syncthreads();
 
-  // the merge kernel may be scheduled now; it waits for this grid's completion before reading
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   if (warp == NC) {
     decode_producer<D, TMA>(a, stages, hdr, full, empty);
   } else if (warp < NC) {
     decode_consumer<D, NT, TMA>(a, stages, hdr, full, empty, mbuf);
   }
+  // Only now may the merge kernel be scheduled (it waits for this grid's completion before
+  // reading).  Triggered at the start, its CTAs would sit in their wait for the whole decode and
+  // hold the thread slots that kernels on other streams (an extend beside the decode) need on
+  // the SMs this grid does not use or has finished with.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -721,9 +724,18 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 }
 
 // ---------------------------------------------------------------------------------------------
-// Generic merge_states: one warp per (row, head).
+// Generic merge_states: one warp per (row, head); partial states in fp32 or bf16.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) merge_states_kernel(const float* __restrict__ o_parts,
+__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__ o_parts,
                                                            const float* __restrict__ lse_parts,
                                                            int32_t S, int64_t rows_heads, int32_t D,
                                                            __nv_bfloat16* __restrict__ out,
@@ -748,7 +760,7 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const float* __restri
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < S; ++s) {
       const float w = __expf(__ldg(lse_parts + (int64_t)s * rows_heads + rh) - mx);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * rows_heads + rh) * D + d));
+      const float4 v = load4(o_parts + ((int64_t)s * rows_heads + rh) * D + d);
       acc.x += w * v.x;
       acc.y += w * v.y;
       acc.z += w * v.z;
@@ -875,15 +887,26 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
                             const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             uint32_t* err_word, void* stream) {
-  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0) return PKV_ERR_INVALID_ARG;
+  return pkv_paged_decode_ctas(pool, q, batch_size, num_q_heads, kv_indptr, kv_indices, kv_lens,
+                               sm_scale, out, lse, workspace, workspace_bytes, err_word, 0, stream);
+}
+
+pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                 int32_t num_q_heads, const int32_t* kv_indptr,
+                                 const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 uint32_t* err_word, int32_t max_ctas, void* stream) {
+  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || max_ctas < 0)
+    return PKV_ERR_INVALID_ARG;
   if (batch_size == 0) return PKV_OK;
   if (!q || !kv_indptr || !kv_indices || !kv_lens || !out) return PKV_ERR_INVALID_ARG;
   if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (batch_size > 0x7fffffff / 64) return PKV_ERR_UNSUPPORTED;
   const int D = pool->head_dim;
-  const int ncta = pkv_host::sm_count();
+  int ncta = pkv_host::sm_count();
   if (ncta <= 0) return PKV_ERR_CUDA;
+  if (max_ctas > 0 && max_ctas < ncta) ncta = max_ctas;  // fewer partials: the workspace still fits
   DecodePlan p;
   if (!make_plan(batch_size, num_q_heads, pool->num_kv_heads, D, ncta, p, pool->page_size, pool->num_pages))
     return PKV_ERR_UNSUPPORTED;
@@ -945,9 +968,14 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
   return p.NT == 1 ? launch_decode<64, 1, false>(p, a, st) : launch_decode<64, 2, false>(p, a, st);
 }
 
-pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
-                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
-                            float* lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+template <typename T>
+pkv_status launch_merge_states(const T* o_parts, const float* lse_parts, int32_t num_splits,
+                               int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                               float* lse, void* stream) {
   if (num_splits < 0 || num_rows < 0 || num_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
   if (num_rows == 0) return PKV_OK;
   if (!o_parts || !lse_parts || !out || num_splits == 0) return PKV_ERR_INVALID_ARG;
@@ -957,9 +985,27 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
   const int warps = 8;
   const int64_t blocks = (rh + warps - 1) / warps;
   if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-  merge_states_kernel<<<(unsigned)blocks, warps * 32, 0, (cudaStream_t)stream>>>(
+  merge_states_kernel<T><<<(unsigned)blocks, warps * 32, 0, (cudaStream_t)stream>>>(
       o_parts, lse_parts, num_splits, rh, head_dim, (__nv_bfloat16*)out, lse);
   return pkv_host::launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
+                            int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                            float* lse, void* stream) {
+  return launch_merge_states(o_parts, lse_parts, num_splits, num_rows, num_heads, head_dim, out, lse,
+                             stream);
+}
+
+pkv_status pkv_merge_states_bf16(const void* o_parts, const float* lse_parts, int32_t num_splits,
+                                 int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
+                                 float* lse, void* stream) {
+  return launch_merge_states((const __nv_bfloat16*)o_parts, lse_parts, num_splits, num_rows, num_heads,
+                             head_dim, out, lse, stream);
 }
 
 }  // extern "C"

@@ -89,10 +89,19 @@ struct ExtendArgs {
   int32_t tokens_per_tile;
   float scale_log2;
   const int32_t* order;  // request of grid z-index z, longest KV first (nullable: batch order)
+  // shared-prefix parts (the unmasked instance): part b's rows q_start[b] .. + q_len[b] of q attend to all
+  // prefix_lens[b] positions of its page list and write rows o_start[b] .. of out
+  const int32_t* q_start;
+  const int32_t* o_start;
+  const int32_t* q_len;
+  int32_t num_q_rows;    // rows of q
+  int32_t num_out_rows;  // rows of out
 };
 
 struct Work {
-  int h, b, qo0, E, t0, P, L, kv_end, n_tiles;
+  // q0 / qo0: first query row of the request in q / in out; row i of the request sees the KV
+  // positions j <= min(mask0 + i, L - 1)
+  int h, b, q0, qo0, E, t0, mask0, L, kv_end, n_tiles;
 };
 
 // Producer warp: Q once, then K and V tiles page by page.  Lane i issues box i of a tile; the
@@ -106,8 +115,8 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   const int G = a.group;
   if (kv == 0 && lane == 0) {
     mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-    tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.qo0 + w.t0, &bars->q_full);
-    tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.qo0 + w.t0, &bars->q_full);
+    tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.q0 + w.t0, &bars->q_full);
+    tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.q0 + w.t0, &bars->q_full);
   }
   const int p0 = __ldg(a.kv_indptr + w.b);
   const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
@@ -255,8 +264,8 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   const int tok = w.t0 + (r >> a.log2_group);
   const int g = r & (G - 1);
   const bool valid = tok < w.E;
-  const int limit = min(w.P + tok, w.L - 1);  // last visible KV position of this row
-  const int min_limit = w.P + w.t0;            // smallest limit over the tile's rows
+  const int limit = min(w.mask0 + tok, w.L - 1);        // last visible KV position of this row
+  const int min_limit = min(w.mask0 + w.t0, w.L - 1);  // smallest limit over the tile's rows
   // scores are scaled inside one FFMA, x = s * scale - m * scale; with a non-positive scale the
   // max of s is not the max of the scaled scores, so scale first
   const bool pos_scale = a.scale_log2 > 0.f;
@@ -410,6 +419,7 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
 }
 
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Work w;
@@ -417,18 +427,49 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
   w.h = blockIdx.y;
   w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
-  w.qo0 = __ldg(a.qo_indptr + w.b);
-  w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
+  if (kCausal) {
+    w.qo0 = __ldg(a.qo_indptr + w.b);
+    w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
+    w.q0 = w.qo0;
+  } else {
+    w.q0 = __ldg(a.q_start + w.b);
+    w.qo0 = __ldg(a.o_start + w.b);
+    w.E = __ldg(a.q_len + w.b);
+  }
   if (w.t0 >= w.E) return;  // uniform: this tile has no rows
+  if (w.q0 < 0 || w.qo0 < 0 || w.q0 > a.num_q_rows - w.E || w.qo0 > a.num_out_rows - w.E) {
+    if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_ROW_OOB);
+    return;
+  }
+  const int P = __ldg(a.prefix_lens + w.b);
+  if (kCausal) {
+    w.mask0 = P;
+    w.L = P + w.E;
+    w.kv_end = P + min(w.t0 + a.tokens_per_tile, w.E);
+  } else {
+    // every row sees the part's whole KV
+    w.L = max(P, 0);
+    w.mask0 = w.L;
+    w.kv_end = w.L;
+    if (P < 0 && threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_LENGTH);
+  }
+  w.n_tiles = (w.kv_end + kBN - 1) / kBN;
+  if (w.n_tiles == 0) {  // a part with no KV: o = 0, lse = -inf (uniform over the CTA)
+    const int G = a.group;
+    const int rows = min(a.tokens_per_tile, w.E - w.t0) * G;
+    for (int i = threadIdx.x; i < rows * (kHD / 8); i += kThreads) {
+      const int row = i / (kHD / 8), c = i % (kHD / 8);
+      const int64_t orow = (int64_t)(w.qo0 + w.t0 + row / G) * a.num_q_heads + (int64_t)w.h * G + row % G;
+      reinterpret_cast<uint4*>(a.out + orow * kHD)[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (c == 0 && a.lse) a.lse[orow] = -INFINITY;
+    }
+    return;
+  }
   const uint32_t sb = smem_u32(smem);
   if (sb & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_INTERNAL);
     return;
   }
-  w.P = __ldg(a.prefix_lens + w.b);
-  w.L = w.P + w.E;
-  w.kv_end = w.P + min(w.t0 + a.tokens_per_tile, w.E);
-  w.n_tiles = (w.kv_end + kBN - 1) / kBN;
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -488,9 +529,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   }
 }
 
-// Requests ordered by KV length (prefix + new tokens), longest first and ties by index, so that
-// the grid dispatches the CTAs with the most work first and the last wave holds short ones: a
-// bitonic sort of (length, index) keys in shared memory by one CTA.  n is a power of two >= B.
+// Requests ordered by KV length (prefix + new tokens; a shared-prefix part's whole KV when
+// qo_indptr is null), longest first and ties by index, so that the grid dispatches the CTAs with
+// the most work first and the last wave holds short ones: a bitonic sort of (length, index) keys
+// in shared memory by one CTA.  n is a power of two >= B.
 constexpr int kMaxOrdered = 4096;
 
 __global__ void __launch_bounds__(1024) extend_order_kernel(const int32_t* __restrict__ qo_indptr,
@@ -501,7 +543,7 @@ __global__ void __launch_bounds__(1024) extend_order_kernel(const int32_t* __res
     unsigned long long k = 0;  // padding sorts last
     if (i < B) {
       const int64_t L = (int64_t)max(0, __ldg(prefix_lens + i)) +
-                        max(0, __ldg(qo_indptr + i + 1) - __ldg(qo_indptr + i));
+                        (qo_indptr ? max(0, __ldg(qo_indptr + i + 1) - __ldg(qo_indptr + i)) : 0);
       const unsigned long long len = (unsigned long long)min(L, (int64_t)0x7fffffff);
       k = (len << 32) | (0xffffffffull - (unsigned)i);  // larger first; equal lengths by index
     }
@@ -553,19 +595,42 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
   return ((size_t)batch_size * 4 + 255) & ~(size_t)255;
 }
 
-pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
-                            const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
-                            const int32_t* kv_indptr, const int32_t* kv_indices,
-                            const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
-                            void* out, float* lse, void* workspace, size_t workspace_bytes,
-                            uint32_t* err_word, void* stream) {
-  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || num_q_tokens < 0 ||
-      max_extend_len < 0)
+}  // extern "C"
+
+namespace {
+
+template <bool kCausal>
+pkv_status launch_kernel(const ExtendArgs& a, dim3 grid, cudaStream_t stream) {
+  // whether this instance's dynamic shared-memory limit was raised on this device (any host thread)
+  static std::atomic<bool> configured[64];
+  const int dev = pkv_host::current_device();
+  if (dev < 0) return PKV_ERR_CUDA;
+  if (dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
+    if (cudaFuncSetAttribute(paged_extend_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) configured[dev].store(true, std::memory_order_relaxed);
+  }
+  paged_extend_kernel<kCausal><<<grid, kThreads, kSmemBytes, stream>>>(a);
+  return pkv_host::launch_status();
+}
+
+// The launch shared by the extend (causal) and the shared-prefix parts (causal == 0):
+// the host checks, the tensor maps, the request order and the kernel.
+pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows, int32_t num_out_rows,
+                         const int32_t* qo_indptr, const int32_t* q_start, const int32_t* o_start,
+                         const int32_t* q_len, int causal, int32_t batch_size, int32_t num_q_heads,
+                         const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_lens,
+                         int32_t max_rows, float sm_scale, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, uint32_t* err_word, void* stream) {
+  if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || num_q_rows < 0 ||
+      num_out_rows < 0 || max_rows < 0)
     return PKV_ERR_INVALID_ARG;
-  if (batch_size == 0 || num_q_tokens == 0 || max_extend_len == 0) return PKV_OK;
-  if (!q || !qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (batch_size == 0 || num_q_rows == 0 || num_out_rows == 0 || max_rows == 0) return PKV_OK;
+  if (!q || !kv_indptr || !kv_indices || !kv_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (causal ? !qo_indptr : (!q_start || !o_start || !q_len)) return PKV_ERR_INVALID_ARG;
   const size_t ws_need = pkv_extend_workspace_size(batch_size, num_q_heads, pool->num_kv_heads,
-                                                   pool->head_dim, max_extend_len);
+                                                   pool->head_dim, max_rows);
   if (ws_need > 0 && (!workspace || workspace_bytes < ws_need)) return PKV_ERR_WORKSPACE;
   if (ws_need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
   if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
@@ -584,14 +649,14 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
   const uint64_t Hq = num_q_heads, Hkv = pool->num_kv_heads;
   const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
   const uint32_t R = pool->page_size < kBN ? pool->page_size : kBN;
-  if (!pkv_host::encode_tmap_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_tokens, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
+  if (!pkv_host::encode_tmap_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_rows, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
       !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R) ||
       !pkv_host::encode_tmap_3d(&a.tm_v, pool->v, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R))
     return PKV_ERR_CUDA;
   a.qo_indptr = qo_indptr;
   a.kv_indptr = kv_indptr;
   a.kv_indices = kv_indices;
-  a.prefix_lens = prefix_lens;
+  a.prefix_lens = kv_lens;
   a.out = (__nv_bfloat16*)out;
   a.lse = lse;
   a.err_word = err_word;
@@ -604,30 +669,58 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
   a.tokens_per_tile = tpt;
   a.scale_log2 = sm_scale * kLog2e;
   a.order = nullptr;
+  a.q_start = q_start;
+  a.o_start = o_start;
+  a.q_len = q_len;
+  a.num_q_rows = num_q_rows;
+  a.num_out_rows = num_out_rows;
   if (ws_need > 0) {
     int n = 1;
     while (n < batch_size) n <<= 1;
-    extend_order_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(qo_indptr, prefix_lens, batch_size, n,
-                                                              (int32_t*)workspace);
+    extend_order_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(causal ? qo_indptr : nullptr, kv_lens,
+                                                              batch_size, n, (int32_t*)workspace);
     const pkv_status st = pkv_host::launch_status();
     if (st != PKV_OK) return st;
     a.order = (const int32_t*)workspace;
   }
 
-  // whether the kernel's dynamic shared-memory limit was raised on this device (any host thread)
-  static std::atomic<bool> configured[64];
-  const int dev = pkv_host::current_device();
-  if (dev < 0) return PKV_ERR_CUDA;
-  if (dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(paged_extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    if (dev < 64) configured[dev].store(true, std::memory_order_relaxed);
-  }
-  const int tiles = (max_extend_len + tpt - 1) / tpt;
+  const int tiles = (max_rows + tpt - 1) / tpt;
   dim3 grid(tiles, pool->num_kv_heads, batch_size);
-  paged_extend_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(a);
-  return pkv_host::launch_status();
+  return causal ? launch_kernel<true>(a, grid, (cudaStream_t)stream)
+                : launch_kernel<false>(a, grid, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
+                            const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
+                            const int32_t* kv_indptr, const int32_t* kv_indices,
+                            const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            uint32_t* err_word, void* stream) {
+  return launch_extend(pool, q, num_q_tokens, num_q_tokens, qo_indptr, nullptr, nullptr, nullptr, 1,
+                       batch_size, num_q_heads, kv_indptr, kv_indices, prefix_lens, max_extend_len,
+                       sm_scale, out, lse, workspace, workspace_bytes, err_word, stream);
+}
+
+size_t pkv_shared_prefix_workspace_size(int32_t num_parts, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t max_part_rows) {
+  return pkv_extend_workspace_size(num_parts, num_q_heads, num_kv_heads, head_dim, max_part_rows);
+}
+
+pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int32_t num_q_rows,
+                                       const int32_t* q_start, const int32_t* q_len,
+                                       const int32_t* o_start, int32_t num_parts, int32_t num_q_heads,
+                                       const int32_t* kv_indptr, const int32_t* kv_indices,
+                                       const int32_t* kv_lens, int32_t max_part_rows, float sm_scale,
+                                       void* o_part, float* lse_part, int32_t num_out_rows,
+                                       void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                                       void* stream) {
+  return launch_extend(pool, q, num_q_rows, num_out_rows, nullptr, q_start, o_start, q_len, 0,
+                       num_parts, num_q_heads, kv_indptr, kv_indices, kv_lens, max_part_rows, sm_scale,
+                       o_part, lse_part, workspace, workspace_bytes, err_word, stream);
 }
 
 }  // extern "C"

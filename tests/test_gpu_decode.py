@@ -170,3 +170,28 @@ def test_decode_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         lib.paged_decode(torch.zeros((1, 8, 96), dtype=torch.bfloat16, device="cuda"), kp96, kp96, *args)
     assert e.value.status == 2  # head_dim 96 not built
+
+
+@pytest.mark.parametrize("max_ctas", [1, 5, 100, 100000])
+def test_decode_on_fewer_sms(lib, max_ctas):
+    # the persistent grid limited to max_ctas SMs (the rest left to other streams): a different
+    # split of the token stream, the same attention within tolerance; a limit at or above the SM
+    # count is the ordinary decode, bit for bit
+    b = random_small_batch(12, page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                           decode_lens=(5000, 1, 700, 12000, 33, 2500), share_decode_prefix=512)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    kpd, vpd = kp.cuda(), vp.cuda()
+    out, lse = run_decode(lib, b, kpd, vpd, max_ctas=max_ctas)
+    o_ref, lse_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices,
+                                         b.dec_kv_lens, 16, b.sm_scale)
+    assert_attention_close(out, lse, o_ref, lse_ref, what=f"decode on {max_ctas} SMs")
+    if max_ctas >= torch.cuda.get_device_properties(0).multi_processor_count:
+        o2, l2 = run_decode(lib, b, kpd, vpd)
+        assert torch.equal(out.view(torch.int16), o2.view(torch.int16)) and torch.equal(lse, l2)
+
+
+def test_decode_negative_sm_limit_rejected(lib):
+    b = random_small_batch(13, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=64, decode_lens=(20,))
+    with pytest.raises(lib.PagedKVError) as e:
+        run_decode(lib, b, b.k_pool.cuda(), b.v_pool.cuda(), max_ctas=-1)
+    assert e.value.status == 1

@@ -89,6 +89,8 @@ def test_two_branch_step_matches_serial_and_oracle(lib):
     ews = torch.empty(max(256, lib.extend_workspace_size(b.num_extend, 32, 8, 128, b.max_extend_len)),
                       dtype=torch.uint8, device="cuda")
     fork, join = torch.cuda.Event(), torch.cuda.Event()
+    # the decode leaves 16 SMs to the extend beside it, as the benchmark's branched step does
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count - 16
 
     def run(branches):
         d = DeviceBatch(b)
@@ -104,7 +106,8 @@ def test_two_branch_step_matches_serial_and_oracle(lib):
                 st2.wait_event(fork)
             lib.kv_append(d.k_pool, d.v_pool, d.k_new[:nd], d.v_new[:nd], d.slot_mapping[:nd], stream=st)
             lib.paged_decode(d.dec_q, d.k_pool, d.v_pool, d.dec_kv_indptr, d.dec_kv_indices,
-                             d.dec_kv_lens, b.sm_scale, out=d_out, lse=d_lse, workspace=dws, stream=st)
+                             d.dec_kv_lens, b.sm_scale, out=d_out, lse=d_lse, workspace=dws, stream=st,
+                             max_ctas=ctas)
             lib.kv_append(d.k_pool, d.v_pool, d.k_new[nd:], d.v_new[nd:], d.slot_mapping[nd:],
                           stream=s_ext)
             lib.paged_extend(d.ext_q, d.k_pool, d.v_pool, d.ext_qo_indptr, d.ext_kv_indptr,

@@ -15,4 +15,5 @@ from .paged import (  # noqa: F401
     CONFIG_NAMES,
     random_small_batch,
     make_spec_verify,
+    make_shared_prefix_decode,
 )

@@ -304,6 +304,23 @@ def make_spec_verify(num_requests: int = 64, draft_tokens: int = 5, seed: int = 
                              page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128)
 
 
+def make_shared_prefix_decode(num_requests: int = 256, shared_tokens: int = 4096,
+                              seed: int = SEED_BASE + 7) -> PagedBatch:
+    """A decode batch whose requests all continue one long shared prompt: every request shares the
+    pages of its first ``shared_tokens`` positions (a radix-cache hit on a common system prompt
+    or parallel samples of one prompt: mini-sglang README, "KVcache Management") and owns
+    U[64, 1024] further positions, the last one appended this step.  Qwen3-8B attention shape,
+    page 16.  The requests are consecutive, so the shared-prefix (cascade) decode can take them
+    as one group."""
+    gen = torch.Generator().manual_seed(seed)
+    reqs = [RequestSpec("decode", shared_tokens + own, 1, share_group=0)
+            for own in _ri(gen, 64, 1024, num_requests)]
+    return build_paged_batch(gen, reqs, name=f"shared-prefix decode: {num_requests} requests sharing a "
+                             f"{shared_tokens}-token prefix, own KV U[64,1024], 32q/8kv heads, D=128, "
+                             "page 16", page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             shared_tokens={0: shared_tokens})
+
+
 def random_small_batch(
     seed: int,
     *,
