@@ -743,8 +743,11 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
   const int64_t rh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (rh >= rows_heads) return;
+  // lane i holds the LSEs of splits i, i + 32, ...: the max and the sum are warp reductions
   float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(lse_parts + (int64_t)s * rows_heads + rh));
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldg(lse_parts + (int64_t)s * rows_heads + rh));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   __nv_bfloat16* op = out + rh * D;
   if (mx == -INFINITY) {  // every split empty
     for (int d = lane * 4; d < D; d += 128)
@@ -754,22 +757,48 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
     return;
   }
   float tot = 0.f;
-  for (int s = 0; s < S; ++s) tot += __expf(__ldg(lse_parts + (int64_t)s * rows_heads + rh) - mx);
-  const float inv = 1.f / tot;
-  for (int d = lane * 4; d < D; d += 128) {
+  // every lane runs every iteration (the shuffles need the whole warp); lanes past D only load
+  // and store nothing
+  for (int d0 = 0; d0 < D; d0 += 128) {
+    const int d = d0 + lane * 4;
+    const bool has = d < D;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float w = __expf(__ldg(lse_parts + (int64_t)s * rows_heads + rh) - mx);
-      const float4 v = load4(o_parts + ((int64_t)s * rows_heads + rh) * D + d);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    float part = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int n = min(32, S - s0);
+      // this lane's split weight, shared with the warp by shuffles
+      const float wl = lane < n ? __expf(__ldg(lse_parts + (int64_t)(s0 + lane) * rows_heads + rh) - mx) : 0.f;
+      part += wl;
+      for (int i = 0; i < n; i += 4) {
+        float4 v[4];
+        float w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // four splits' loads in flight
+          w[k] = __shfl_sync(0xffffffffu, wl, (i + k) & 31);
+          v[k] = has && i + k < n ? load4(o_parts + ((int64_t)(s0 + i + k) * rows_heads + rh) * D + d)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (i + k < n && w[k] != 0.f) {  // an empty split adds nothing, whatever its o holds
+            acc.x += w[k] * v[k].x;
+            acc.y += w[k] * v[k].y;
+            acc.z += w[k] * v[k].z;
+            acc.w += w[k] * v[k].w;
+          }
+        }
+      }
     }
-    op[d + 0] = __float2bfloat16_rn(acc.x * inv);
-    op[d + 1] = __float2bfloat16_rn(acc.y * inv);
-    op[d + 2] = __float2bfloat16_rn(acc.z * inv);
-    op[d + 3] = __float2bfloat16_rn(acc.w * inv);
+    tot = part;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (has) {
+      const float inv = 1.f / tot;
+      op[d + 0] = __float2bfloat16_rn(acc.x * inv);
+      op[d + 1] = __float2bfloat16_rn(acc.y * inv);
+      op[d + 2] = __float2bfloat16_rn(acc.z * inv);
+      op[d + 3] = __float2bfloat16_rn(acc.w * inv);
+    }
   }
   if (lane == 0 && lse) lse[rh] = mx + logf(tot);
 }
