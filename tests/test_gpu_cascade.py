@@ -145,3 +145,28 @@ def test_cascade_decode_matches_oracle(lib, case):
     o_ref, l_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
                                        b.page_size, b.sm_scale, requests=check)
     assert_attention_close(out, lse, o_ref, l_ref, rows=np.array(check), what=f"cascade {case}")
+
+
+@pytest.mark.slow
+def test_cascade_full_shared_prefix_workload(lib):
+    """The shared-prefix workload at full size (256 decodes over a 4096-token shared prefix), planned
+    as the benchmark plans it, on a sample of requests."""
+    from workloads import make_shared_prefix_decode
+
+    b = make_shared_prefix_decode()
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = plan_shared_prefix(b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens, [(0, b.num_decode)],
+                              b.page_size, num_kv_heads=b.num_kv_heads,
+                              group_size=b.num_q_heads // b.num_kv_heads, num_sms=sms)
+    assert plan.shared_tokens == [4096] and plan.num_splits > 1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.cascade_decode(b.dec_q.cuda(), kp.cuda(), vp.cuda(), plan.to("cuda"), b.sm_scale,
+                                  err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rng = np.random.default_rng(1)
+    sample = sorted(rng.choice(b.num_decode, 24, replace=False).tolist())
+    o_ref, l_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens,
+                                       b.page_size, b.sm_scale, requests=sample)
+    assert_attention_close(out, lse, o_ref, l_ref, rows=np.array(sample), what="cascade, full workload")

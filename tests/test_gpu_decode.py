@@ -68,12 +68,15 @@ def test_decode_long_context_split(lib):
 
 
 @pytest.mark.slow
-def test_decode_mixed_step_decodes(lib):
-    """The 256 decodes of the mixed step (64 share a prefix), on a sample of requests."""
+@pytest.mark.parametrize("spare_sms", [0, 16])
+def test_decode_mixed_step_decodes(lib, spare_sms):
+    """The 256 decodes of the mixed step (64 share a prefix), on a sample of requests; also on
+    all but 16 SMs, as the benchmark's branched step runs it beside the extend."""
     b, kp, vp = config_with_append(5)
     d = DeviceBatch(b)
     lib.kv_append(d.k_pool, d.v_pool, d.k_new, d.v_new, d.slot_mapping)
-    out, lse = run_decode(lib, b, d.k_pool, d.v_pool)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out, lse = run_decode(lib, b, d.k_pool, d.v_pool, max_ctas=sms - spare_sms if spare_sms else 0)
     rng = np.random.default_rng(0)
     sample = sorted(rng.choice(b.num_decode, 64, replace=False).tolist())
     o_ref, lse_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices,
