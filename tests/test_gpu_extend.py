@@ -191,3 +191,21 @@ def test_extend_speculative_verify_shape(lib):
     qo = b.ext_qo_indptr.tolist()
     rows = [i for r in sample for i in range(qo[r], qo[r + 1])]
     assert_attention_close(out, lse, o_ref, lse_ref, rows=rows, what="spec verify")
+
+
+@pytest.mark.slow
+def test_extend_more_requests_than_the_plan_sorts(lib):
+    # 4500 requests: above the 4096 the plan kernel sorts in shared memory, so they keep batch
+    # order, and the item prefix is scanned in several chunks; a sample is checked
+    ext = [((i * 13) % 90, 1 + (i * 7) % 3) for i in range(4500)]
+    b = random_small_batch(77, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=ext)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_extend(lib, b, kp, vp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    sample = list(range(0, 4500, 97)) + [4095, 4096, 4499]
+    o_ref, lse_ref = oracle_extend(b, kp, vp, requests=sample)
+    qo = b.ext_qo_indptr.tolist()
+    rows = np.concatenate([np.arange(qo[r], qo[r + 1]) for r in sample])
+    assert_attention_close(out, lse, o_ref, lse_ref, rows=rows, what="4500 requests")
