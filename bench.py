@@ -32,7 +32,6 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode KV GB/s (% HBM peak); extend TFLOP/s (% bf16 peak); attn tokens/s"
-WORKLOAD_IDX = 5
 
 
 def _peaks():
@@ -636,11 +635,7 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v, seeded lengths and page permutation)",
         "config": {
-            "workload": (b.name if args.workload != "mixed" else
-                         "mixed continuous-batching step: kv_append 2304 tokens + paged decode of 256 "
-                         "requests (KV U[512,4096], 64 share a 2048-token prefix) + ragged extend of 4x512 "
-                         "chunked-prefill tokens (prefixes 0/512/1024/1536); Qwen3-8B attention 32q/8kv "
-                         "heads, head_dim 128, page 16"),
+            "workload": workload_label(args.workload, b),
             "decode_requests": b.num_decode, "extend_requests": b.num_extend,
             "new_tokens": b.num_new_tokens, "page_size": b.page_size, "num_pages": b.num_pages,
             "l2": ("L2 flushed (256 MB written) before every step" if args.flush_l2 else
@@ -732,13 +727,21 @@ def cpu_baseline(b, seconds=12.0, threads=0):
                       f"BLAS and torch limited to {cores} threads"}
 
 
+def workload_label(name, b):
+    """The workload as the JSON line's config names it (the same for both arms)."""
+    if name != "mixed":
+        return b.name
+    return ("mixed continuous-batching step: kv_append 2304 tokens + paged decode of 256 requests (KV "
+            "U[512,4096], 64 share a 2048-token prefix) + ragged extend of 4x512 chunked-prefill tokens "
+            "(prefixes 0/512/1024/1536); Qwen3-8B attention 32q/8kv heads, head_dim 128, page 16")
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
-    from workloads import make_config
     import oracle
 
-    b = make_config(WORKLOAD_IDX)
+    b = load_workload(args.workload)
     kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
     run = _oracle_sample_runner(b, kp, vp)
     for k in range(args.warmup):
@@ -758,9 +761,10 @@ def run_reference(args, ws, rank):
             "n_gpus": ws, "steps": args.steps, "steps_completed": done, "warmup": args.warmup,
             "ms_per_step": round(el / done * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "mixed continuous-batching step (bounded oracle sample per step)"},
+            "config": {"workload": workload_label(args.workload, b) + " (a bounded oracle sample per step)"},
             "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": "per step: 1 decode request + up to 8 extend query rows of the mixed step"},
+                             "sample": "per step: 1 decode request (all heads) and/or up to 8 extend query "
+                                       "rows of one request of this workload"},
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
