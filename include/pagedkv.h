@@ -77,6 +77,16 @@ const char* pkv_status_string(pkv_status s);
 int32_t pkv_version(void);
 
 /*
+ * Check of the kernels' failure path: one GPU thread waits on an mbarrier that nothing ever
+ * arrives on, with the bounded wait every kernel of this library uses (0.5 s of %globaltimer),
+ * then gives up and ORs PKV_DEVERR_TIMEOUT into *err_word (device uint32, required).  The launch
+ * returns at once; after the stream synchronises the word holds the bit and the context stays
+ * usable.  It exists so that tests can show that a wait that never completes ends with an error
+ * status instead of a hang.
+ */
+pkv_status pkv_selftest_bounded_wait(uint32_t* err_word, void* stream);
+
+/*
  * KV-cache write.  For t < num_tokens: pool.k row slot_mapping[t] = k_new[t] and the same for
  * V; a negative slot marks a padding token and writes nothing.  A bit-exact copy.
  *   k_new, v_new  bf16 [num_tokens, num_kv_heads, head_dim] (device)

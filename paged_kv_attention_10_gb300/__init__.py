@@ -21,7 +21,7 @@ __all__ = [
     "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
     "paged_decode", "paged_decode_noalloc", "extend_workspace_size", "paged_extend",
     "merge_states", "shared_prefix_workspace_size", "shared_prefix_attention", "cascade_decode",
-    "status_string", "version", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB",
+    "status_string", "version", "selftest_bounded_wait", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB",
     "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT", "DEVERR_INTERNAL", "DEVERR_ROW_OOB",
 ]
 
@@ -85,6 +85,7 @@ def load():
         "pkv_rope_kv_append": (_c_i32, [P, _vp, _vp, _vp, _vp, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp]),
         "pkv_paged_decode_noalloc": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
                                               _vp, _vp]),
+        "pkv_selftest_bounded_wait": (_c_i32, [_vp, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -92,6 +93,15 @@ def load():
         f.argtypes = args
     _lib = lib
     return lib
+
+
+def selftest_bounded_wait(err_word, stream=None) -> None:
+    """Run the bounded-wait check: a GPU wait that nothing completes gives up after its limit and
+    ORs DEVERR_TIMEOUT into err_word (int32 [1] on the device)."""
+    _need(err_word, "err_word", torch.int32)
+    dev = err_word.device
+    with torch.cuda.device(dev):
+        _call("pkv_selftest_bounded_wait", _ptr(err_word), _stream_ptr(stream, dev))
 
 
 def status_string(status: int) -> str:

@@ -91,3 +91,26 @@ const char* pkv_status_string(pkv_status s) {
 int32_t pkv_version(void) { return 100; }  // 0.1.0
 
 }  // extern "C"
+
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on, with the same bounded wait the
+// kernels use, and reports the timeout the way they do.
+__global__ void bounded_wait_selftest_kernel(uint32_t* err_word) {
+  __shared__ uint64_t bar;
+  pkv::mbar_init(&bar, 1);
+  pkv::fence_mbar_init();
+  if (!pkv::mbar_wait(&bar, 0)) pkv::report(err_word, PKV_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_selftest_bounded_wait(uint32_t* err_word, void* stream) {
+  if (!err_word) return PKV_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(err_word);
+  return pkv_host::launch_status();
+}
+
+}  // extern "C"

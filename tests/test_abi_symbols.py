@@ -48,6 +48,9 @@ def test_host_only_calls(cdll):
     cdll.pkv_status_string.restype = ctypes.c_char_p
     assert cdll.pkv_status_string(0) == b"ok"
     assert cdll.pkv_status_string(3) == b"workspace too small"
+    # the bounded-wait check rejects a missing error word before launching anything
+    cdll.pkv_selftest_bounded_wait.restype = ctypes.c_int32
+    assert cdll.pkv_selftest_bounded_wait(None, None) == 1
 
 
 def test_null_pool_is_rejected_before_any_cuda_call(cdll):
