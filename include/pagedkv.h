@@ -77,6 +77,29 @@ const char* pkv_status_string(pkv_status s);
 int32_t pkv_version(void);
 
 /*
+ * Host-side checks of step metadata, on HOST copies, before they go to the device: what the
+ * kernels would otherwise only report through the error word (or, for duplicate slots, not at
+ * all).  Both return PKV_OK, or PKV_ERR_INVALID_ARG with the first offending request / token in
+ * *bad_request / *bad_token (nullable; -1 when none).
+ *
+ * pkv_validate_page_table: kv_indptr[0] == 0 and non-decreasing; every listed page index in
+ * [0, num_pages); min_len <= kv_lens[b] <= (kv_indptr[b+1] - kv_indptr[b]) * page_size (min_len
+ * 1 for a decode; for an extend pass the KV lengths prefix + new tokens and min_len 1).
+ *   kv_indptr int32 [batch_size+1], kv_indices int32 [kv_indptr[batch_size]], kv_lens int32
+ *   [batch_size] (host)
+ *
+ * pkv_validate_slots: every slot < num_slots (= num_pages * page_size); negative slots are
+ * padding; no slot written twice (the append's caller contract).  *bad_token is the first
+ * out-of-range token, else the first token whose slot an earlier token already writes.
+ *   slot_mapping int64 [num_tokens] (host)
+ */
+pkv_status pkv_validate_page_table(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* kv_lens, int32_t batch_size, int64_t num_pages,
+                                   int32_t page_size, int32_t min_len, int32_t* bad_request);
+pkv_status pkv_validate_slots(const int64_t* slot_mapping, int32_t num_tokens, int64_t num_slots,
+                              int32_t* bad_token);
+
+/*
  * Check of the kernels' failure path: one GPU thread waits on an mbarrier that nothing ever
  * arrives on, with the bounded wait every kernel of this library uses (0.5 s of %globaltimer),
  * then gives up and ORs PKV_DEVERR_TIMEOUT into *err_word (device uint32, required).  The launch

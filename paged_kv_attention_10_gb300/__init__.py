@@ -21,8 +21,9 @@ __all__ = [
     "load", "library_path", "PagedKVError", "kv_append", "paged_gather", "decode_workspace_size",
     "paged_decode", "paged_decode_noalloc", "extend_workspace_size", "paged_extend",
     "merge_states", "shared_prefix_workspace_size", "shared_prefix_attention", "cascade_decode",
-    "status_string", "version", "selftest_bounded_wait", "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB",
-    "DEVERR_SLOT_OOB", "DEVERR_LENGTH", "DEVERR_TIMEOUT", "DEVERR_INTERNAL", "DEVERR_ROW_OOB",
+    "status_string", "version", "selftest_bounded_wait", "validate_page_table", "validate_slots",
+    "rope_cos_sin_table", "rope_kv_append", "DEVERR_PAGE_OOB", "DEVERR_SLOT_OOB", "DEVERR_LENGTH",
+    "DEVERR_TIMEOUT", "DEVERR_INTERNAL", "DEVERR_ROW_OOB",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +87,8 @@ def load():
         "pkv_paged_decode_noalloc": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
                                               _vp, _vp]),
         "pkv_selftest_bounded_wait": (_c_i32, [_vp, _vp]),
+        "pkv_validate_page_table": (_c_i32, [_vp, _vp, _vp, _c_i32, _c_i64, _c_i32, _c_i32, _vp]),
+        "pkv_validate_slots": (_c_i32, [_vp, _c_i32, _c_i64, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -93,6 +96,44 @@ def load():
         f.argtypes = args
     _lib = lib
     return lib
+
+
+def _host_i(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous host {dtype} tensor")
+    return t
+
+
+def validate_page_table(kv_indptr, kv_indices, kv_lens, num_pages: int, page_size: int,
+                        min_len: int = 1) -> None:
+    """Check host page-table metadata before it goes to the device; raises PagedKVError naming
+    the first bad request (``.bad``)."""
+    _host_i(kv_indptr, "kv_indptr", torch.int32)
+    _host_i(kv_indices, "kv_indices", torch.int32)
+    _host_i(kv_lens, "kv_lens", torch.int32)
+    B = kv_lens.numel()
+    if kv_indptr.numel() != B + 1:
+        raise ValueError("kv_indptr must have batch_size + 1 entries")
+    bad = ctypes.c_int32(-1)
+    st = load().pkv_validate_page_table(_ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_lens), B,
+                                        int(num_pages), int(page_size), int(min_len), ctypes.byref(bad))
+    if st != 0:
+        e = PagedKVError(f"pkv_validate_page_table (request {bad.value})", st)
+        e.bad = bad.value
+        raise e
+
+
+def validate_slots(slot_mapping, num_slots: int) -> None:
+    """Check a host slot mapping (in range, no slot twice); raises PagedKVError naming the first
+    bad token (``.bad``)."""
+    _host_i(slot_mapping, "slot_mapping", torch.int64)
+    bad = ctypes.c_int32(-1)
+    st = load().pkv_validate_slots(_ptr(slot_mapping), slot_mapping.numel(), int(num_slots),
+                                   ctypes.byref(bad))
+    if st != 0:
+        e = PagedKVError(f"pkv_validate_slots (token {bad.value})", st)
+        e.bad = bad.value
+        raise e
 
 
 def selftest_bounded_wait(err_word, stream=None) -> None:

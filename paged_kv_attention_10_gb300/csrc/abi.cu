@@ -1,7 +1,10 @@
 // C-ABI plumbing: status strings, version, host-side argument checks and device properties.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
+#include <utility>
+#include <vector>
 
 #include "tc05.cuh"
 
@@ -106,6 +109,58 @@ __global__ void bounded_wait_selftest_kernel(uint32_t* err_word) {
 }  // namespace
 
 extern "C" {
+
+pkv_status pkv_validate_page_table(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* kv_lens, int32_t batch_size, int64_t num_pages,
+                                   int32_t page_size, int32_t min_len, int32_t* bad_request) {
+  if (bad_request) *bad_request = -1;
+  if (batch_size < 0 || num_pages < 0 || page_size <= 0 || min_len < 0) return PKV_ERR_INVALID_ARG;
+  if (batch_size == 0) return PKV_OK;
+  if (!kv_indptr || !kv_lens || (!kv_indices && kv_indptr[batch_size] > 0)) return PKV_ERR_INVALID_ARG;
+  auto bad = [&](int32_t b) {
+    if (bad_request) *bad_request = b;
+    return PKV_ERR_INVALID_ARG;
+  };
+  if (kv_indptr[0] != 0) return bad(0);
+  for (int32_t b = 0; b < batch_size; ++b) {
+    const int64_t lo = kv_indptr[b], hi = kv_indptr[b + 1];
+    if (hi < lo) return bad(b);
+    const int64_t len = kv_lens[b];
+    if (len < min_len || len > (hi - lo) * (int64_t)page_size) return bad(b);
+    for (int64_t k = lo; k < hi; ++k)
+      if (kv_indices[k] < 0 || kv_indices[k] >= num_pages) return bad(b);
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_validate_slots(const int64_t* slot_mapping, int32_t num_tokens, int64_t num_slots,
+                              int32_t* bad_token) {
+  if (bad_token) *bad_token = -1;
+  if (num_tokens < 0 || num_slots < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!slot_mapping) return PKV_ERR_INVALID_ARG;
+  std::vector<std::pair<int64_t, int32_t>> used;  // (slot, token) of every non-padding token
+  used.reserve((size_t)num_tokens);
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;  // padding
+    if (s >= num_slots) {
+      if (bad_token) *bad_token = t;
+      return PKV_ERR_INVALID_ARG;
+    }
+    used.emplace_back(s, t);
+  }
+  std::sort(used.begin(), used.end());
+  int32_t first_dup = -1;  // the later token of the earliest duplicated pair, in token order
+  for (size_t i = 1; i < used.size(); ++i)
+    if (used[i].first == used[i - 1].first && (first_dup < 0 || used[i].second < first_dup))
+      first_dup = used[i].second;
+  if (first_dup >= 0) {
+    if (bad_token) *bad_token = first_dup;
+    return PKV_ERR_INVALID_ARG;
+  }
+  return PKV_OK;
+}
 
 pkv_status pkv_selftest_bounded_wait(uint32_t* err_word, void* stream) {
   if (!err_word) return PKV_ERR_INVALID_ARG;

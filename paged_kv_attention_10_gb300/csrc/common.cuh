@@ -7,9 +7,22 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pagedkv.h"
 
 #define PKV_DEV __device__ __forceinline__
+
+namespace pkv_host {
+// An NVTX range named after the ABI call, open for the call's duration, so that a profiler's
+// timeline shows each library call around its kernels (NVTX costs nothing without a profiler).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace pkv_host
 
 namespace pkv {
 

@@ -916,6 +916,7 @@ pkv_status pkv_paged_decode(const pkv_pool* pool, const void* q, int32_t batch_s
                             const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             uint32_t* err_word, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_decode");
   return pkv_paged_decode_ctas(pool, q, batch_size, num_q_heads, kv_indptr, kv_indices, kv_lens,
                                sm_scale, out, lse, workspace, workspace_bytes, err_word, 0, stream);
 }
@@ -925,6 +926,7 @@ pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t ba
                                  const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  uint32_t* err_word, int32_t max_ctas, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_decode_ctas");
   if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || max_ctas < 0)
     return PKV_ERR_INVALID_ARG;
   if (batch_size == 0) return PKV_OK;
@@ -1026,6 +1028,7 @@ extern "C" {
 pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_t num_splits,
                             int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
                             float* lse, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_merge_states");
   return launch_merge_states(o_parts, lse_parts, num_splits, num_rows, num_heads, head_dim, out, lse,
                              stream);
 }
@@ -1033,6 +1036,7 @@ pkv_status pkv_merge_states(const float* o_parts, const float* lse_parts, int32_
 pkv_status pkv_merge_states_bf16(const void* o_parts, const float* lse_parts, int32_t num_splits,
                                  int32_t num_rows, int32_t num_heads, int32_t head_dim, void* out,
                                  float* lse, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_merge_states_bf16");
   return launch_merge_states((const __nv_bfloat16*)o_parts, lse_parts, num_splits, num_rows, num_heads,
                              head_dim, out, lse, stream);
 }
@@ -1080,6 +1084,7 @@ extern "C" pkv_status pkv_paged_decode_noalloc(const pkv_pool* pool, const void*
                                                const int32_t* kv_indices, const int32_t* kv_lens,
                                                float sm_scale, void* out, float* lse,
                                                uint32_t* err_word, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_decode_noalloc");
   if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0) return PKV_ERR_INVALID_ARG;
   if (batch_size == 0) return PKV_OK;
   const int n = pkv_host::sm_count();

@@ -700,6 +700,7 @@ pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_t
                             const int32_t* prefix_lens, int32_t max_extend_len, float sm_scale,
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             uint32_t* err_word, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_extend");
   return launch_extend(pool, q, num_q_tokens, num_q_tokens, qo_indptr, nullptr, nullptr, nullptr, 1,
                        batch_size, num_q_heads, kv_indptr, kv_indices, prefix_lens, max_extend_len,
                        sm_scale, out, lse, workspace, workspace_bytes, err_word, stream);
@@ -718,6 +719,7 @@ pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int3
                                        void* o_part, float* lse_part, int32_t num_out_rows,
                                        void* workspace, size_t workspace_bytes, uint32_t* err_word,
                                        void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_shared_prefix_attention");
   return launch_extend(pool, q, num_q_rows, num_out_rows, nullptr, q_start, o_start, q_len, 0,
                        num_parts, num_q_heads, kv_indptr, kv_indices, kv_lens, max_part_rows, sm_scale,
                        o_part, lse_part, workspace, workspace_bytes, err_word, stream);

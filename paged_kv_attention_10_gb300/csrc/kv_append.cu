@@ -79,6 +79,7 @@ extern "C" {
 pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int32_t num_tokens, uint32_t* err_word,
                          void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_kv_append");
   if (!pkv_host::valid_pool(pool) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
@@ -99,6 +100,7 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
 pkv_status pkv_paged_gather(const pkv_pool* pool, const int32_t* kv_indptr,
                             const int32_t* kv_indices, const int32_t* kv_lens, int32_t batch_size,
                             void* k_out, void* v_out, uint32_t* err_word, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_gather");
   if (!pkv_host::valid_pool(pool) || batch_size < 0) return PKV_ERR_INVALID_ARG;
   if (batch_size == 0) return PKV_OK;
   if (!kv_indptr || !kv_indices || !kv_lens || !k_out || !v_out) return PKV_ERR_INVALID_ARG;

@@ -97,6 +97,7 @@ extern "C" pkv_status pkv_rope_kv_append(const pkv_pool* pool, const void* k_new
                                          const float* cos_sin, int32_t max_position, void* q,
                                          int32_t num_q_heads, int32_t num_tokens, uint32_t* err_word,
                                          void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_rope_kv_append");
   if (!pkv_host::valid_pool(pool) || num_tokens < 0 || num_q_heads < 0 || max_position <= 0)
     return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
