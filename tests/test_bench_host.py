@@ -42,6 +42,44 @@ def test_workload_counts_by_brute_force():
     assert c["attn_tokens"] == 3 + qo[-1]
 
 
+def test_extend_bytes_and_cascade_counts_by_brute_force():
+    from paged_kv_attention_10_gb300.cascade import plan_shared_prefix
+
+    b = random_small_batch(4, page_size=4, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                           decode_lens=(21, 30, 26, 7), extend=((8, 4), (0, 6)),
+                           share_decode_prefix=16, share_extend_prefix=8)
+    c = bench.workload_counts(b)
+    row = 2 * 16 * 2  # one token's K (or V) row: Hkv x D x bf16
+    # extend: each physical slot of the extend requests once (the shared prefix once), K and V,
+    # plus q in, out and lse, plus the page lists
+    seen = set()
+    ind, idx = b.ext_kv_indptr.tolist(), b.ext_kv_indices.tolist()
+    qo = b.ext_qo_indptr.tolist()
+    for r, P in enumerate(b.ext_prefix_lens.tolist()):
+        for j in range(P + qo[r + 1] - qo[r]):
+            seen.add(idx[ind[r] + j // 4] * 4 + j % 4)
+    meta = (len(ind) + len(idx) + 2 * len(qo) - 1) * 4
+    assert c["extend_bytes"] == len(seen) * row * 2 + qo[-1] * 4 * (16 * 2 * 2 + 4) + meta
+    # cascade: the shared-prefix parts' unmasked pairs, the own-pages decode's unique slots
+    sharers = [i for i, r in enumerate(b.requests) if r.kind == "decode" and r.share_group == 0]
+    assert sharers == [0, 1, 2]
+    plan = plan_shared_prefix(b.dec_kv_indptr, b.dec_kv_indices, b.dec_kv_lens, [(0, 3)], 4,
+                              num_kv_heads=2, group_size=2, num_sms=1, min_chunk_tokens=4)
+    cc = bench.cascade_counts(b, plan)
+    assert plan.shared_tokens == [16]
+    assert cc["prefix_flops"] == 4 * 16 * 4 * (3 * 16)  # 3 queries x 16 shared positions, all heads
+    own = set()
+    sptr, sidx = plan.suffix_kv_indptr.tolist(), plan.suffix_kv_indices.tolist()
+    for r, L in enumerate(plan.suffix_kv_lens.tolist()):
+        for j in range(L):
+            own.add(sidx[sptr[r] + j // 4] * 4 + j % 4)
+    B = b.num_decode
+    meta = (len(sptr) + len(sidx) + B) * 4
+    assert cc["suffix_bytes"] == len(own) * row * 2 + B * 4 * (16 * 2 * 2 + 4) + meta
+    S = plan.num_splits
+    assert cc["merge_bytes"] == (S + 2) * B * 4 * (16 * 2 + 4)
+
+
 def _worker(rank, world, port, q):
     import torch.distributed as dist
 
