@@ -786,6 +786,10 @@ def load_workload(name):
         from workloads import make_shared_prefix_decode
 
         return make_shared_prefix_decode()
+    if name == "small-prefill":
+        from workloads import make_small_prefill
+
+        return make_small_prefill()
     if name == "profile":
         from workloads import random_small_batch
 
@@ -798,7 +802,8 @@ def load_workload(name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="mixed",
-                    choices=sorted(WORKLOADS) + ["spec-verify", "shared-prefix-decode", "profile"])
+                    choices=sorted(WORKLOADS) + ["spec-verify", "shared-prefix-decode", "small-prefill",
+                                                 "profile"])
     ap.add_argument("--cascade", action="store_true",
                     help="decode through the shared-prefix (cascade) plan: the shared pages once per "
                          "group on tensor cores, each request's own pages, and a merge")

@@ -242,7 +242,8 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
  *   workspace  device, 16-byte aligned, at least pkv_extend_workspace_size(...) bytes, caller-owned
  *              and not shared with a call in flight on another stream (may be NULL when that
  *              size is 0); smaller returns PKV_ERR_WORKSPACE
- * head_dim 128, page_size a power of two >= 8; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ * head_dim 64 or 128, page_size a power of two >= 8, num_q_heads / num_kv_heads from 1 to 16 (a Q
+ * tile holds group x floor(128 / group) rows of (token, query head) pairs).
  */
 pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
                             const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
@@ -270,14 +271,14 @@ size_t pkv_shared_prefix_workspace_size(int32_t num_parts, int32_t num_q_heads, 
  * the extend; the part's output rows are o_start[p] .. o_start[p] + q_len[p] - 1 of o_part:
  *   o_part[r, h, :] = sum_j softmax_j(scale * q . k_j) v_j,  lse_part[r, h] = ln sum_j exp(scale * q . k_j)
  * A part with kv_lens[p] == 0 writes o = 0 and lse = -inf (an empty split for the merge).
- *   q          bf16 [num_q_rows, num_q_heads, 128] (device)
+ *   q          bf16 [num_q_rows, num_q_heads, head_dim] (device)
  *   q_start, q_len, o_start, kv_lens  int32 [num_parts]; kv_indptr int32 [num_parts+1] (device)
  *   max_part_rows  an upper bound of q_len[p] (sizes the grid; rows beyond it are not computed)
- *   o_part     bf16 [num_out_rows, num_q_heads, 128]; lse_part nullable fp32 [num_out_rows, num_q_heads]
+ *   o_part     bf16 [num_out_rows, num_q_heads, head_dim]; lse_part nullable fp32 [num_out_rows, num_q_heads]
  *   workspace  as for pkv_paged_extend, pkv_shared_prefix_workspace_size(...) bytes
  *   err_word   nullable; PKV_DEVERR_ROW_OOB for a part whose rows fall outside q or o_part (the part
  *              is skipped), PKV_DEVERR_PAGE_OOB / PKV_DEVERR_LENGTH as for the extend
- * head_dim 128, page_size a power of two >= 8, group size in {1, 2, 4, 8, 16}.  Parts that write
+ * head_dim 64 or 128, page_size a power of two >= 8, group size 1 to 16.  Parts that write
  * the same output rows race; different parts may read the same query rows.
  */
 pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int32_t num_q_rows,

@@ -81,9 +81,9 @@ def plan_shared_prefix(kv_indptr, kv_indices, kv_lens, groups, page_size: int, *
     lens = np.asarray(kv_lens, dtype=np.int64)
     B = lens.size
     ps = int(page_size)
-    if indptr.size != B + 1 or ps <= 0 or group_size <= 0 or _TILE_ROWS % group_size:
+    if indptr.size != B + 1 or ps <= 0 or not 1 <= group_size <= 16:
         raise ValueError("bad page lists, page size or group size")
-    tpt = _TILE_ROWS // group_size
+    tpt = _TILE_ROWS // group_size  # tokens per Q tile (group x tpt <= 128 rows)
     owner = np.full(B, -1, dtype=np.int64)
     kept = []  # (first, count, shared pages)
     for first, count in groups:

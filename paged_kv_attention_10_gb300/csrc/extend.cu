@@ -39,24 +39,30 @@ using namespace pkv;
 
 constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
 constexpr int kBN = 64;   // KV positions per tile
-constexpr int kHD = 128;  // head_dim
 // warp 0 Q/K loads, warp 1 QK MMAs, warps 2..9 softmax, warp 10 V loads, warp 11 PV MMAs
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 256); S buffers at [0,64) and [64,128)
+constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 128 + D); S buffers at [0,64) and [64,128)
+constexpr uint32_t kQHalf = kBM * 128;   // one 64-dim half of the Q tile, 16 KB
+constexpr uint32_t kKVHalf = kBN * 128;  // 64 positions x 64 dims, 8 KB
 
-constexpr uint32_t kQBytes = kBM * kHD * 2;  // 32 KB, two 64-column halves
-constexpr uint32_t kQHalf = kQBytes / 2;
-constexpr uint32_t kKVHalf = kBN * 128;      // 64 positions x 64 dims, 8 KB
-constexpr uint32_t kKVStage = 2 * kKVHalf;   // 16 KB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
-constexpr uint32_t kOffX = kOffV + 2 * kKVStage;  // row-max exchange [tile parity][half][row]
-constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [half][row]
-constexpr uint32_t kOffBar = kOffL + 2 * kBM * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 256;
+// Shared-memory layout for head_dim D (64 or 128): operands are stored as 64-dim halves of
+// 128-byte swizzled rows.
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kQBytes = kHalves * kQHalf;  // also the O staging tile (128 rows x 2D bytes)
+  static constexpr uint32_t kKVStage = kHalves * kKVHalf;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kQBytes;
+  static constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
+  static constexpr uint32_t kOffX = kOffV + 2 * kKVStage;   // row-max exchange [tile parity][half][row]
+  static constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [half][row]
+  static constexpr uint32_t kOffBar = kOffL + 2 * kBM * 4;
+  static constexpr uint32_t kSmemBytes = kOffBar + 256;
+  static constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of an O row
+};
 
 struct Bars {
   uint64_t q_full;
@@ -85,7 +91,8 @@ struct ExtendArgs {
   int32_t log2_ps;
   int32_t num_q_heads;
   int32_t group;
-  int32_t log2_group;
+  int32_t rows_used;   // group * tokens_per_tile <= 128 Q-tile rows hold (token, head) pairs
+  int32_t log2_group;  // log2(group) when the group is a power of two, else -1 (divide)
   int32_t tokens_per_tile;
   float scale_log2;
   const int32_t* order;  // request of grid z-index z, longest KV first (nullable: batch order)
@@ -110,13 +117,17 @@ struct Work {
 // kv = 0: the K warp (also loads Q); kv = 1: the V warp.  Separate warps keep the K stream
 // ahead of the QK MMAs even while the V stream waits for its stage to be freed by PV.  The
 // warp returns only when its copies have landed (bounded waits).
+template <int D>
 __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
+  using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
   const int G = a.group;
   if (kv == 0 && lane == 0) {
-    mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-    tma_load_3d(sb + kOffQ, &a.tm_q, 0, w.h * G, w.q0 + w.t0, &bars->q_full);
-    tma_load_3d(sb + kOffQ + kQHalf, &a.tm_q, 64, w.h * G, w.q0 + w.t0, &bars->q_full);
+    // one box per 64-dim half: [64 dims x G heads x tokens_per_tile tokens], rows_used rows
+    mbar_arrive_expect_tx(&bars->q_full, C::kHalves * a.rows_used * 128);
+#pragma unroll
+    for (int hf = 0; hf < C::kHalves; ++hf)
+      tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * G, w.q0 + w.t0, &bars->q_full);
   }
   const int p0 = __ldg(a.kv_indptr + w.b);
   const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
@@ -162,12 +173,12 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
       ok = false;
       break;
     }
-    if (lane == 0) mbar_arrive_expect_tx(&fulls[st], nload * R * 128 * 2);
+    if (lane == 0) mbar_arrive_expect_tx(&fulls[st], nload * R * 128 * C::kHalves);
     __syncwarp();
     if (row >= 0) {
-      const uint32_t dst = sb + (kv ? kOffV : kOffK) + st * kKVStage + lane * R * 128;
-      tma_load_3d(dst, tm, 0, w.h, row, &fulls[st]);
-      tma_load_3d(dst + kKVHalf, tm, 64, w.h, row, &fulls[st]);
+      const uint32_t dst = sb + (kv ? C::kOffV : C::kOffK) + st * C::kKVStage + lane * R * 128;
+#pragma unroll
+      for (int hf = 0; hf < C::kHalves; ++hf) tma_load_3d(dst + hf * kKVHalf, tm, hf * 64, w.h, row, &fulls[st]);
     }
     issued = j + 1;
   }
@@ -182,7 +193,9 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
 // wakes when its phase completes:  the QK thread issues QK(j) once K(j) has landed and S buffer
 // j&1 is back from PV(j-2) (P is written over S);  the PV thread issues PV(j) once the softmax
 // has written P(j) and V(j) has landed.  Neither stream ever waits behind the other.
+template <int D>
 __device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
+  using C = Cfg<D>;
   constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
   if (!mbar_wait(&bars->q_full, 0)) return false;
   for (int j = 0; j < w.n_tiles; ++j) {
@@ -191,10 +204,10 @@ __device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint
     if (!mbar_wait(&bars->k_full[st], ph)) return false;
     if (!mbar_wait(&bars->s_free[st], ph ^ 1)) return false;
     tc_fence_after();
-    const uint32_t kb = sb + kOffK + st * kKVStage;
+    const uint32_t kb = sb + C::kOffK + st * C::kKVStage;
 #pragma unroll
-    for (int ks = 0; ks < kHD / 16; ++ks) {
-      const uint64_t adesc = smem_desc_sw128(sb + kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint64_t adesc = smem_desc_sw128(sb + C::kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
       const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
       umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
     }
@@ -204,20 +217,22 @@ __device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint
   return true;
 }
 
+template <int D>
 __device__ bool extend_mma_pv(Bars* bars, uint32_t sb, uint32_t tmem, const Work& w) {
-  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, kHD, true);
+  using C = Cfg<D>;
+  constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
   for (int j = 0; j < w.n_tiles; ++j) {
     const int st = j & 1;
     const uint32_t ph = (j >> 1) & 1;
     if (!mbar_wait(&bars->p_full[st], ph)) return false;
     if (!mbar_wait(&bars->v_full[st], ph)) return false;
     tc_fence_after();
-    const uint32_t vb = sb + kOffV + st * kKVStage;
+    const uint32_t vb = sb + C::kOffV + st * C::kKVStage;
 #pragma unroll
     for (int ks = 0; ks < kBN / 16; ++ks) {
       // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs.
-      // V rows [16ks, 16ks+16) as one MN-major operand of N = 128; its two 64-dim halves are
-      // kKVHalf apart.
+      // V rows [16ks, 16ks+16) as one MN-major operand of N = D; its 64-dim halves are kKVHalf
+      // apart.
       const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
       const uint64_t bdesc = smem_desc_sw128(vb + ks * 2048, kKVHalf, 1024);
       umma_ts(tmem + kColO, pa, bdesc, idesc_pv, j > 0 || ks > 0);
@@ -252,8 +267,10 @@ __device__ __forceinline__ void pair_bar(int wq) {
   }
 }
 
+template <int D>
 __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, uint32_t tmem,
                                const Work& w) {
+  using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;            // TMEM lane quadrant this warp may access
   const int hsel = (warp - 2) >> 2;   // which half of the tile's columns this warp owns
@@ -261,16 +278,17 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   const int tid = (warp - 2) * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
   const int G = a.group;
-  const int tok = w.t0 + (r >> a.log2_group);
-  const int g = r & (G - 1);
-  const bool valid = tok < w.E;
+  const int rt = a.log2_group >= 0 ? r >> a.log2_group : r / G;  // the row's token in the tile
+  const int tok = w.t0 + rt;
+  const int g = r - rt * G;
+  const bool valid = r < a.rows_used && tok < w.E;
   const int limit = min(w.mask0 + tok, w.L - 1);        // last visible KV position of this row
   const int min_limit = min(w.mask0 + w.t0, w.L - 1);  // smallest limit over the tile's rows
   // scores are scaled inside one FFMA, x = s * scale - m * scale; with a non-positive scale the
   // max of s is not the max of the scaled scores, so scale first
   const bool pos_scale = a.scale_log2 > 0.f;
   const float sc = pos_scale ? a.scale_log2 : 1.f;
-  float* xbuf = reinterpret_cast<float*>(smem + kOffX);
+  float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
   float m_used = -INFINITY;  // running max of the scaled (log2) scores
   float l = 0.f;             // this half's running sum
   bool ok = true;
@@ -335,9 +353,9 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
       tc_fence_after();
       {
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int ch = 0; ch < D / 64; ++ch) {
           float o[32];
-          const uint32_t oc = taddr + kColO + hsel * 64 + ch * 32;
+          const uint32_t oc = taddr + kColO + hsel * (D / 2) + ch * 32;
           tmem_ld32(oc, o);
           tmem_wait_ld();
 #pragma unroll
@@ -353,10 +371,10 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j >> 1) & 1));
       if (!ok) break;
       const int r0 = w.kv_end - pos0;
-      const int nchunks = (kBN - r0) * 8 * 2;  // rows x 16-byte chunks x halves
-      uint8_t* vb = smem + kOffV + st * kKVStage;
+      const int nchunks = (kBN - r0) * 8 * C::kHalves;  // rows x 16-byte chunks x halves
+      uint8_t* vb = smem + C::kOffV + st * C::kKVStage;
       for (int idx = tid; idx < nchunks; idx += kSoftmaxWarps * 32) {
-        const int half = idx & 1, rc = idx >> 1;
+        const int half = idx % C::kHalves, rc = idx / C::kHalves;
         const int row = r0 + (rc >> 3), ch = rc & 7;
         *reinterpret_cast<uint4*>(vb + half * kKVHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
@@ -377,25 +395,26 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
   tc_fence_after();
   // the two halves' sums
-  float* lbuf = reinterpret_cast<float*>(smem + kOffL);
+  float* lbuf = reinterpret_cast<float*>(smem + C::kOffL);
   lbuf[hsel * kBM + r] = l;
   pair_bar(wq);
   const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
   const float inv = 1.f / l_tot;
   // The normalised O tile goes through shared memory so that the stores to `out` are coalesced
   // (a thread owns one row; storing rows directly scatters every warp store over 32 rows).  The
-  // Q buffer is free: every QK has completed.  Row r's 16-byte chunk c sits at chunk c ^ (r % 16)
-  // of its 256-byte line, which spreads a warp's column of chunks over the banks.
-  uint8_t* stage = smem + kOffQ;
+  // Q buffer is free: every QK has completed.  Row r's 16-byte chunk c sits at chunk
+  // c ^ (r % kChunks) of its 2D-byte line, which spreads a warp's column of chunks over the banks.
+  constexpr int kCh = C::kChunks;
+  uint8_t* stage = smem + C::kOffQ;
 #pragma unroll 1
-  for (int ch = 0; ch < 2; ++ch) {
+  for (int ch = 0; ch < D / 64; ++ch) {
     float o[32];
-    tmem_ld32(taddr + kColO + hsel * 64 + ch * 32, o);
+    tmem_ld32(taddr + kColO + hsel * (D / 2) + ch * 32, o);
     tmem_wait_ld();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int c = hsel * 8 + ch * 4 + q;
-      *reinterpret_cast<uint4*>(stage + r * 256 + ((c ^ (r & 15)) << 4)) =
+      const int c = hsel * (kCh / 2) + ch * 4 + q;
+      *reinterpret_cast<uint4*>(stage + r * (kCh * 16) + ((c ^ (r & (kCh - 1))) << 4)) =
           make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
                      pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
                      pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
@@ -405,22 +424,24 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   if (valid && hsel == 0 && a.lse)
     a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l_tot)) * kLn2;
   softmax_bar();
-  // 128 rows x 16 chunks: a warp stores two whole 256-byte rows per instruction
+  // 128 rows x kCh chunks: a warp stores whole 2D-byte rows per instruction
 #pragma unroll
-  for (int k = 0; k < kBM * 16 / (kSoftmaxWarps * 32); ++k) {
+  for (int k = 0; k < kBM * kCh / (kSoftmaxWarps * 32); ++k) {
     const int i = tid + k * kSoftmaxWarps * 32;
-    const int row = i >> 4, c = i & 15;
-    const int t = w.t0 + (row >> a.log2_group);
-    if (t < w.E) {
-      const int64_t orow = (int64_t)(w.qo0 + t) * a.num_q_heads + (int64_t)w.h * G + (row & (G - 1));
-      reinterpret_cast<uint4*>(a.out + orow * kHD)[c] =
-          *reinterpret_cast<const uint4*>(stage + row * 256 + ((c ^ (row & 15)) << 4));
+    const int row = i / kCh, c = i % kCh;
+    const int tr = a.log2_group >= 0 ? row >> a.log2_group : row / G;
+    const int t = w.t0 + tr;
+    if (row < a.rows_used && t < w.E) {
+      const int64_t orow = (int64_t)(w.qo0 + t) * a.num_q_heads + (int64_t)w.h * G + (row - tr * G);
+      reinterpret_cast<uint4*>(a.out + orow * D)[c] =
+          *reinterpret_cast<const uint4*>(stage + row * (kCh * 16) + ((c ^ (row & (kCh - 1))) << 4));
     }
   }
 }
 
-template <bool kCausal>
+template <bool kCausal, int D>
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
+  using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Work w;
   // later tiles of a request attend over more positions: launch them first
@@ -457,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   if (w.n_tiles == 0) {  // a part with no KV: o = 0, lse = -inf (uniform over the CTA)
     const int G = a.group;
     const int rows = min(a.tokens_per_tile, w.E - w.t0) * G;
-    for (int i = threadIdx.x; i < rows * (kHD / 8); i += kThreads) {
-      const int row = i / (kHD / 8), c = i % (kHD / 8);
+    for (int i = threadIdx.x; i < rows * (D / 8); i += kThreads) {
+      const int row = i / (D / 8), c = i % (D / 8);
       const int64_t orow = (int64_t)(w.qo0 + w.t0 + row / G) * a.num_q_heads + (int64_t)w.h * G + row % G;
-      reinterpret_cast<uint4*>(a.out + orow * kHD)[c] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(a.out + orow * D)[c] = make_uint4(0u, 0u, 0u, 0u);
       if (c == 0 && a.lse) a.lse[orow] = -INFINITY;
     }
     return;
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     if (threadIdx.x == 0) report(a.err_word, PKV_DEVERR_INTERNAL);
     return;
   }
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -502,10 +523,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0 || warp == 10) {
-    extend_producer(a, sb, bars, w, warp == 0 ? 0 : 1);
+    extend_producer<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
   } else if (warp == 1) {
     if (lane == 0) {
-      if (!extend_mma_qk(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      if (!extend_mma_qk<D>(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
       // its MMAs have completed before TMEM is released (immediate on the normal path)
       umma_commit(&bars->qk_done);
       if (!mbar_wait(&bars->qk_done, 0)) report(a.err_word, PKV_DEVERR_TIMEOUT);
@@ -513,13 +534,13 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     __syncwarp();
   } else if (warp == 11) {
     if (lane == 0) {
-      if (!extend_mma_pv(bars, sb, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      if (!extend_mma_pv<D>(bars, sb, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
       umma_commit(&bars->pv_done);
       if (!mbar_wait(&bars->pv_done, 0)) report(a.err_word, PKV_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else {
-    extend_softmax(a, smem, bars, tmem, w);
+    extend_softmax<D>(a, smem, bars, tmem, w);
   }
   tc_fence_before();
   __syncthreads();
@@ -599,19 +620,20 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
 
 namespace {
 
-template <bool kCausal>
+template <bool kCausal, int D>
 pkv_status launch_kernel(const ExtendArgs& a, dim3 grid, cudaStream_t stream) {
+  constexpr uint32_t smem = Cfg<D>::kSmemBytes;
   // whether this instance's dynamic shared-memory limit was raised on this device (any host thread)
   static std::atomic<bool> configured[64];
   const int dev = pkv_host::current_device();
   if (dev < 0) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(paged_extend_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(paged_extend_kernel<kCausal, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_relaxed);
   }
-  paged_extend_kernel<kCausal><<<grid, kThreads, kSmemBytes, stream>>>(a);
+  paged_extend_kernel<kCausal, D><<<grid, kThreads, smem, stream>>>(a);
   return pkv_host::launch_status();
 }
 
@@ -635,12 +657,12 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   if (ws_need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
   if (!pkv_host::aligned16(q) || !pkv_host::aligned16(out)) return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
-  if (pool->head_dim != kHD) return PKV_ERR_UNSUPPORTED;
+  const int D = pool->head_dim;
+  if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   const int G = num_q_heads / pool->num_kv_heads;
-  const int lg = log2_exact(G);
   const int lps = log2_exact(pool->page_size);
   // page boxes of at least 8 rows keep every TMA destination on a 1024-byte swizzle atom
-  if (lg < 0 || G > 16 || lps < 3) return PKV_ERR_UNSUPPORTED;
+  if (G > 16 || lps < 3) return PKV_ERR_UNSUPPORTED;
   if (pool->num_pages * (int64_t)pool->page_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   if (batch_size > 65535 || pool->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -649,9 +671,10 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   const uint64_t Hq = num_q_heads, Hkv = pool->num_kv_heads;
   const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
   const uint32_t R = pool->page_size < kBN ? pool->page_size : kBN;
-  if (!pkv_host::encode_tmap_3d(&a.tm_q, q, kHD, Hq, (uint64_t)num_q_rows, kHD * 2, Hq * kHD * 2, 64, G, tpt) ||
-      !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R) ||
-      !pkv_host::encode_tmap_3d(&a.tm_v, pool->v, kHD, Hkv, rows, kHD * 2, Hkv * kHD * 2, 64, 1, R))
+  const uint64_t Db = (uint64_t)D * 2;
+  if (!pkv_host::encode_tmap_3d(&a.tm_q, q, D, Hq, (uint64_t)num_q_rows, Db, Hq * Db, 64, G, tpt) ||
+      !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, D, Hkv, rows, Db, Hkv * Db, 64, 1, R) ||
+      !pkv_host::encode_tmap_3d(&a.tm_v, pool->v, D, Hkv, rows, Db, Hkv * Db, 64, 1, R))
     return PKV_ERR_CUDA;
   a.qo_indptr = qo_indptr;
   a.kv_indptr = kv_indptr;
@@ -665,7 +688,8 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   a.log2_ps = lps;
   a.num_q_heads = num_q_heads;
   a.group = G;
-  a.log2_group = lg;
+  a.rows_used = G * tpt;
+  a.log2_group = log2_exact(G);
   a.tokens_per_tile = tpt;
   a.scale_log2 = sm_scale * kLog2e;
   a.order = nullptr;
@@ -686,8 +710,9 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
 
   const int tiles = (max_rows + tpt - 1) / tpt;
   dim3 grid(tiles, pool->num_kv_heads, batch_size);
-  return causal ? launch_kernel<true>(a, grid, (cudaStream_t)stream)
-                : launch_kernel<false>(a, grid, (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (D == 128) return causal ? launch_kernel<true, 128>(a, grid, st) : launch_kernel<false, 128>(a, grid, st);
+  return causal ? launch_kernel<true, 64>(a, grid, st) : launch_kernel<false, 64>(a, grid, st);
 }
 
 }  // namespace

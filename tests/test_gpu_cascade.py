@@ -15,22 +15,23 @@ from _gpu_helpers import assert_attention_close
 pytestmark = pytest.mark.gpu
 
 
-def _pool_batch(seed, ps, Hq, Hkv, lens):
+def _pool_batch(seed, ps, Hq, Hkv, lens, D=128):
     """Page lists of the given lengths over a NaN-filled pool (unused slots poison any stray read)."""
-    b = random_small_batch(seed, page_size=ps, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+    b = random_small_batch(seed, page_size=ps, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                            decode_lens=lens, decode_new=0)
     return b
 
 
-@pytest.mark.parametrize("ps,Hq,Hkv", [(16, 32, 8), (8, 8, 8), (64, 16, 2), (32, 16, 16)])
-def test_shared_prefix_parts_match_oracle(lib, ps, Hq, Hkv):
+@pytest.mark.parametrize("ps,Hq,Hkv,D", [(16, 32, 8, 128), (8, 8, 8, 128), (64, 16, 2, 128), (32, 16, 16, 128),
+                                         (16, 14, 2, 64), (16, 12, 2, 128)])
+def test_shared_prefix_parts_match_oracle(lib, ps, Hq, Hkv, D):
     lens = (700, 64, 129, 1, 300, 2000)
-    b = _pool_batch(90 + ps + Hq, ps, Hq, Hkv, lens)
+    b = _pool_batch(90 + ps + Hq, ps, Hq, Hkv, lens, D)
     G = Hq // Hkv
     tpt = 128 // G
     g = torch.Generator().manual_seed(ps * 7 + Hq)
     Nq = 3 * tpt + 5
-    q = torch.randn((Nq, Hq, 128), generator=g).to(torch.bfloat16)
+    q = torch.randn((Nq, Hq, D), generator=g).to(torch.bfloat16)
     # parts: (q_start, q_len, kv length used of page list p); list 3 is cut to 0 (an empty part)
     spec = [(0, Nq, 700), (5, 2 * tpt + 1, 64), (tpt - 3, 7, 129), (Nq - 1, 1, 0), (1, tpt, 300),
             (2, tpt + 9, 1999)]
@@ -47,7 +48,7 @@ def test_shared_prefix_parts_match_oracle(lib, ps, Hq, Hkv):
     o_ref, l_ref = oracle.shared_prefix_attention(q, kp, vp, i32(q_start), i32(q_len), i32(o_start),
                                                   b.dec_kv_indptr, b.dec_kv_indices, i32(kv_lens),
                                                   n_out, ps, b.sm_scale)
-    o = torch.full((n_out, Hq, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = torch.full((n_out, Hq, D), 7.0, dtype=torch.bfloat16, device="cuda")
     l = torch.full((n_out, Hq), 7.0, dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = lambda t: t.cuda()

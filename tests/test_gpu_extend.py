@@ -112,6 +112,33 @@ def test_extend_property_sweep(lib, case):
     assert_attention_close(out, lse, o_ref, lse_ref, what=str(case))
 
 
+# any group size up to 16 (the Q tile then holds group x floor(128 / group) rows) and head_dim 64
+GENERAL = [
+    # (page_size, Hq, Hkv, head_dim, [(prefix, extend), ...])
+    (16, 14, 2, 64, [(0, 37), (100, 70), (511, 1), (16, 18)]),  # Qwen2.5-0.5B attention: group 7
+    (16, 6, 2, 128, [(0, 50), (77, 43), (3, 1)]),                # group 3: 126 rows
+    (32, 20, 4, 128, [(64, 26), (0, 100)]),                      # group 5: 125 rows
+    (8, 12, 2, 64, [(9, 22), (0, 21), (130, 5)]),                # group 6, page 8
+    (16, 16, 16, 64, [(0, 129), (200, 64)]),                     # group 1, head_dim 64
+    (64, 64, 4, 64, [(63, 17), (1, 8)]),                         # group 16, head_dim 64
+    (16, 24, 2, 128, [(0, 30), (45, 11)]),                       # group 12: 120 rows
+]
+
+
+@pytest.mark.parametrize("case", GENERAL, ids=[f"ps{c[0]}-q{c[1]}-kv{c[2]}-d{c[3]}" for c in GENERAL])
+def test_extend_any_group_and_head_dim_64(lib, case):
+    ps, hq, hkv, d, ext = case
+    b = random_small_batch(300 + ps + hq + d, page_size=ps, num_q_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, extend=ext)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, ps)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_extend(lib, b, kp, vp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what=f"extend {case[:4]}")
+
+
 def test_extend_shared_prefix_pages(lib):
     b = random_small_batch(17, page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
                            extend=[(512, 100), (600, 37), (1000, 256), (40, 50)], share_extend_prefix=512)
@@ -153,10 +180,10 @@ def test_extend_bad_page_index_is_reported(lib):
 
 
 def test_extend_host_checks(lib):
-    b = random_small_batch(20, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=64, extend=[(4, 4)])
+    b = random_small_batch(20, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=96, extend=[(4, 4)])
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
-    assert e.value.status == 2  # head_dim 64 not built for extend
+    assert e.value.status == 2  # head_dim 96 not built
     b = random_small_batch(21, page_size=24, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
@@ -165,10 +192,10 @@ def test_extend_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
     assert e.value.status == 2  # pages smaller than 8 rows
-    b = random_small_batch(22, page_size=16, num_q_heads=6, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
+    b = random_small_batch(22, page_size=16, num_q_heads=34, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
-    assert e.value.status == 2  # group size 3
+    assert e.value.status == 2  # group size 17
     b = random_small_batch(24, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
                            extend=[(4, 4), (0, 9)])
     need = lib.extend_workspace_size(2, 8, 2, 128, b.max_extend_len)
@@ -209,3 +236,18 @@ def test_extend_more_requests_than_the_plan_sorts(lib):
     qo = b.ext_qo_indptr.tolist()
     rows = np.concatenate([np.arange(qo[r], qo[r + 1]) for r in sample])
     assert_attention_close(out, lse, o_ref, lse_ref, rows=rows, what="4500 requests")
+
+
+@pytest.mark.slow
+def test_extend_small_model_prefill_workload(lib):
+    """The small-model prefill workload at full size (Qwen2.5-0.5B attention: group 7, head_dim
+    64), as the benchmark runs it: append, then extend, against the oracle."""
+    from workloads import make_small_prefill
+
+    b = make_small_prefill()
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
+    d = DeviceBatch(b)
+    lib.kv_append(d.k_pool, d.v_pool, d.k_new, d.v_new, d.slot_mapping)
+    out, lse = run_extend(lib, b, d.k_pool, d.v_pool)
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what="small-model prefill")

@@ -16,4 +16,5 @@ from .paged import (  # noqa: F401
     random_small_batch,
     make_spec_verify,
     make_shared_prefix_decode,
+    make_small_prefill,
 )

@@ -304,6 +304,17 @@ def make_spec_verify(num_requests: int = 64, draft_tokens: int = 5, seed: int = 
                              page_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128)
 
 
+def make_small_prefill(num_requests: int = 32, seed: int = SEED_BASE + 8) -> PagedBatch:
+    """The prefill of the nanoSGLang benchmark's prompts for its model: 32 requests with prompts of
+    U[100, 512] tokens and no cached prefix, Qwen2.5-0.5B attention (14 query heads over 2 KV
+    heads, so GQA groups of 7, head_dim 64), page 16 (nanoSGLang README, "Performance")."""
+    gen = torch.Generator().manual_seed(seed)
+    reqs = [RequestSpec("extend", E, E) for E in _ri(gen, 100, 512, num_requests)]
+    return build_paged_batch(gen, reqs, name=f"small-model prefill: {num_requests} prompts of U[100,512] "
+                             "tokens, Qwen2.5-0.5B attention 14q/2kv heads (group 7), D=64, page 16",
+                             page_size=16, num_q_heads=14, num_kv_heads=2, head_dim=64)
+
+
 def make_shared_prefix_decode(num_requests: int = 256, shared_tokens: int = 4096,
                               seed: int = SEED_BASE + 7) -> PagedBatch:
     """A decode batch whose requests all continue one long shared prompt: every request shares the
