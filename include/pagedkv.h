@@ -242,8 +242,9 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
  *   workspace  device, 16-byte aligned, at least pkv_extend_workspace_size(...) bytes, caller-owned
  *              and not shared with a call in flight on another stream (may be NULL when that
  *              size is 0); smaller returns PKV_ERR_WORKSPACE
- * head_dim 64 or 128, page_size a power of two >= 8, num_q_heads / num_kv_heads from 1 to 16 (a Q
- * tile holds group x floor(128 / group) rows of (token, query head) pairs).
+ * head_dim 64 or 128, any page_size (powers of two >= 8 are gathered by TMA boxes, others row by
+ * row), num_q_heads / num_kv_heads from 1 to 16 (a Q tile holds group x floor(128 / group) rows of
+ * (token, query head) pairs).
  */
 pkv_status pkv_paged_extend(const pkv_pool* pool, const void* q, int32_t num_q_tokens,
                             const int32_t* qo_indptr, int32_t batch_size, int32_t num_q_heads,
@@ -278,7 +279,7 @@ size_t pkv_shared_prefix_workspace_size(int32_t num_parts, int32_t num_q_heads, 
  *   workspace  as for pkv_paged_extend, pkv_shared_prefix_workspace_size(...) bytes
  *   err_word   nullable; PKV_DEVERR_ROW_OOB for a part whose rows fall outside q or o_part (the part
  *              is skipped), PKV_DEVERR_PAGE_OOB / PKV_DEVERR_LENGTH as for the extend
- * head_dim 64 or 128, page_size a power of two >= 8, group size 1 to 16.  Parts that write
+ * head_dim 64 or 128, any page_size, group size 1 to 16.  Parts that write
  * the same output rows race; different parts may read the same query rows.
  */
 pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int32_t num_q_rows,

@@ -58,8 +58,8 @@ struct Cfg {
   static constexpr uint32_t kOffK = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
   static constexpr uint32_t kOffX = kOffV + 2 * kKVStage;   // row-max exchange [tile parity][half][row]
-  static constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [half][row]
-  static constexpr uint32_t kOffBar = kOffL + 2 * kBM * 4;
+  static constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [sum][half][row]
+  static constexpr uint32_t kOffBar = kOffL + 2 * 2 * kBM * 4;
   static constexpr uint32_t kSmemBytes = kOffBar + 256;
   static constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of an O row
 };
@@ -103,6 +103,10 @@ struct ExtendArgs {
   const int32_t* q_len;
   int32_t num_q_rows;    // rows of q
   int32_t num_out_rows;  // rows of out
+  // the pool, for the row-copy producer (page sizes that are not a power of two >= 8)
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  int32_t num_kv_heads;
 };
 
 struct Work {
@@ -189,6 +193,102 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   return ok;
 }
 
+// 16-byte asynchronous copies global -> shared (cache in L2 only), committed and waited per
+// group; the producer makes them visible to the tensor cores with a proxy fence.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Producer for any page size (used when it is not a power of two >= 8, page size 1 included): the
+// 64 rows of a K or V tile are copied one token row at a time, two rows per lane, 16 bytes per
+// cp.async, into the same 128-byte-swizzled layout the TMA boxes produce (chunk c of row r at
+// chunk c ^ (r % 8)).  A stage is announced on its full barrier once its copies have landed:
+// after issuing stage j the warp waits for stage j-1's group, fences the async proxy (the MMAs
+// read shared memory through it) and arrives.  The page indices of the next tile are loaded
+// while the current one is copied.  Q still comes by TMA.
+template <int D>
+__device__ bool extend_producer_rows(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
+  using C = Cfg<D>;
+  const int lane = threadIdx.x & 31;
+  const int G = a.group;
+  if (kv == 0 && lane == 0) {
+    mbar_arrive_expect_tx(&bars->q_full, C::kHalves * a.rows_used * 128);
+#pragma unroll
+    for (int hf = 0; hf < C::kHalves; ++hf)
+      tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * G, w.q0 + w.t0, &bars->q_full);
+  }
+  const int p0 = __ldg(a.kv_indptr + w.b);
+  const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
+  const int ps = a.page_size;
+  const __nv_bfloat16* pool = kv ? a.v_pool : a.k_pool;
+  uint64_t* fulls = kv ? bars->v_full : bars->k_full;
+  uint64_t* empties = kv ? bars->v_empty : bars->k_empty;
+  // slot of this lane's row rr of tile j, or -1 (past the KV end, or a bad index, reported)
+  auto slot_of = [&](int j, int rr) -> int64_t {
+    const int pos = j * kBN + lane + 32 * rr;
+    if (j >= w.n_tiles || pos >= w.kv_end) return -1;
+    const int pidx = pos / ps;
+    if (pidx >= np) {
+      report(a.err_word, PKV_DEVERR_LENGTH);
+      return -1;
+    }
+    const int32_t page = __ldg(a.kv_indices + p0 + pidx);
+    if (page < 0 || page >= a.num_pages) {
+      report(a.err_word, PKV_DEVERR_PAGE_OOB);
+      return -1;
+    }
+    return (int64_t)page * ps + (pos - pidx * ps);
+  };
+  int64_t s0 = slot_of(0, 0), s1 = slot_of(0, 1);
+  int issued = 0;
+  bool ok = true;
+  for (int j = 0; j < w.n_tiles; ++j) {
+    const int st = j & 1;
+    const uint32_t ph = (j >> 1) & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(&empties[st], ph ^ 1))) {
+      if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const uint32_t base = sb + (kv ? C::kOffV : C::kOffK) + st * C::kKVStage;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int64_t slot = rr ? s1 : s0;
+      if (slot >= 0) {
+        const int row = lane + 32 * rr;
+        const char* src = reinterpret_cast<const char*>(pool + (slot * a.num_kv_heads + w.h) * D);
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            cp_async16(base + hf * kKVHalf + row * 128 + ((c ^ (row & 7)) << 4), src + hf * 128 + c * 16);
+      }
+    }
+    cp_async_commit();
+    issued = j + 1;
+    s0 = slot_of(j + 1, 0);  // the next tile's rows, while these copies fly
+    s1 = slot_of(j + 1, 1);
+    if (j > 0) {  // the previous stage has landed: publish it
+      cp_async_wait_group<1>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&fulls[(j - 1) & 1]);
+    }
+  }
+  // the last stage issued (also after a timeout: no copy of this warp is left in flight)
+  cp_async_wait_group<0>();
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (issued > 0 && lane == 0) mbar_arrive(&fulls[(issued - 1) & 1]);
+  if (kv == 0) mbar_wait(&bars->q_full, 0);
+  return ok;
+}
+
 // The MMAs are issued by two threads, one per stream, each waiting with a blocking try_wait that
 // wakes when its phase completes:  the QK thread issues QK(j) once K(j) has landed and S buffer
 // j&1 is back from PV(j-2) (P is written over S);  the PV thread issues PV(j) once the softmax
@@ -243,6 +343,26 @@ __device__ bool extend_mma_pv(Bars* bars, uint32_t sb, uint32_t tmem, const Work
   return true;
 }
 
+// Packed pairs of fp32 (sm_100 family): {lo, hi} in one 64-bit register pair.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void split_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 template <int N>
 __device__ __forceinline__ float tree_max(float (&v)[N]) {
 #pragma unroll
@@ -290,7 +410,8 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   const float sc = pos_scale ? a.scale_log2 : 1.f;
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
   float m_used = -INFINITY;  // running max of the scaled (log2) scores
-  float l = 0.f;             // this half's running sum
+  float l = 0.f;             // this half's running sum of the probabilities (for the LSE)
+  float lr = 0.f;            // ... of the probabilities as rounded to bf16 for the PV MMA (for O)
   bool ok = true;
 
   for (int j = 0; j < w.n_tiles; ++j) {
@@ -327,20 +448,31 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     const bool resc = m_new > m_used + 8.f;  // always true on the first tile (m_used = -inf)
     const float m_ref = resc ? m_new : m_used;
     const float corr = resc ? ex2(m_used - m_ref) : 1.f;
+    // Pairs of columns go through Blackwell's packed fp32 arithmetic (one FMA scales two scores,
+    // one add accumulates two probabilities): the exact sum feeds the LSE, the sum of the bf16
+    // values the MMA sees (a bf16 widens exactly by a 16-bit shift) normalises O.
     uint32_t pk[16];
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    uint64_t acc_a = f32x2(0.f, 0.f), acc_b = f32x2(0.f, 0.f), racc_a = f32x2(0.f, 0.f), racc_b = f32x2(0.f, 0.f);
+    const uint64_t sc2 = f32x2(sc, sc), nm2 = f32x2(-m_ref, -m_ref);
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
-      const float p0 = ex2(fmaf(sm[2 * c], sc, -m_ref)), p1 = ex2(fmaf(sm[2 * c + 1], sc, -m_ref));
-      const float p2 = ex2(fmaf(sm[2 * c + 2], sc, -m_ref)), p3 = ex2(fmaf(sm[2 * c + 3], sc, -m_ref));
-      acc0 += p0;
-      acc1 += p1;
-      acc2 += p2;
-      acc3 += p3;
+      float x0, x1, x2, x3;
+      split_f32x2(fma_f32x2(f32x2(sm[2 * c], sm[2 * c + 1]), sc2, nm2), x0, x1);
+      split_f32x2(fma_f32x2(f32x2(sm[2 * c + 2], sm[2 * c + 3]), sc2, nm2), x2, x3);
+      const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+      acc_a = add_f32x2(acc_a, f32x2(p0, p1));
+      acc_b = add_f32x2(acc_b, f32x2(p2, p3));
       pk[c] = pack_bf16x2(p0, p1);
       pk[c + 1] = pack_bf16x2(p2, p3);
+      racc_a = add_f32x2(racc_a, f32x2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)));
+      racc_b = add_f32x2(racc_b, f32x2(__uint_as_float(pk[c + 1] << 16),
+                                       __uint_as_float(pk[c + 1] & 0xffff0000u)));
     }
-    l = l * corr + ((acc0 + acc1) + (acc2 + acc3));
+    float s0, s1, s2, s3;
+    split_f32x2(add_f32x2(acc_a, acc_b), s0, s1);
+    split_f32x2(add_f32x2(racc_a, racc_b), s2, s3);
+    l = l * corr + (s0 + s1);
+    lr = lr * corr + (s2 + s3);
     m_used = m_ref;
     // P (bf16 pairs) over this half's own S columns, which only this warp reads
     tmem_st16(taddr + st * 64 + hsel * 32, pk);
@@ -397,9 +529,12 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   // the two halves' sums
   float* lbuf = reinterpret_cast<float*>(smem + C::kOffL);
   lbuf[hsel * kBM + r] = l;
+  lbuf[(2 + hsel) * kBM + r] = lr;
   pair_bar(wq);
   const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
-  const float inv = 1.f / l_tot;
+  // O is normalised by the sum of the rounded probabilities it was accumulated with, so each
+  // output row is an exact convex combination of V rows (bf16 P then adds no bias of its own)
+  const float inv = 1.f / (lr + lbuf[(2 + (hsel ^ 1)) * kBM + r]);
   // The normalised O tile goes through shared memory so that the stores to `out` are coalesced
   // (a thread owns one row; storing rows directly scatters every warp store over 32 rows).  The
   // Q buffer is free: every QK has completed.  Row r's 16-byte chunk c sits at chunk
@@ -439,7 +574,7 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
 }
 
-template <bool kCausal, int D>
+template <bool kCausal, int D, bool kRows>
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -523,7 +658,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0 || warp == 10) {
-    extend_producer<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
+    if (kRows)
+      extend_producer_rows<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
+    else
+      extend_producer<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
   } else if (warp == 1) {
     if (lane == 0) {
       if (!extend_mma_qk<D>(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
@@ -620,7 +758,7 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
 
 namespace {
 
-template <bool kCausal, int D>
+template <bool kCausal, int D, bool kRows>
 pkv_status launch_kernel(const ExtendArgs& a, dim3 grid, cudaStream_t stream) {
   constexpr uint32_t smem = Cfg<D>::kSmemBytes;
   // whether this instance's dynamic shared-memory limit was raised on this device (any host thread)
@@ -628,12 +766,12 @@ pkv_status launch_kernel(const ExtendArgs& a, dim3 grid, cudaStream_t stream) {
   const int dev = pkv_host::current_device();
   if (dev < 0) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(paged_extend_kernel<kCausal, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(paged_extend_kernel<kCausal, D, kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_relaxed);
   }
-  paged_extend_kernel<kCausal, D><<<grid, kThreads, smem, stream>>>(a);
+  paged_extend_kernel<kCausal, D, kRows><<<grid, kThreads, smem, stream>>>(a);
   return pkv_host::launch_status();
 }
 
@@ -660,9 +798,11 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   const int D = pool->head_dim;
   if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   const int G = num_q_heads / pool->num_kv_heads;
+  if (G > 16) return PKV_ERR_UNSUPPORTED;
+  // page boxes of at least 8 rows keep every TMA destination on a 1024-byte swizzle atom; other
+  // page sizes take the row-copy producer
   const int lps = log2_exact(pool->page_size);
-  // page boxes of at least 8 rows keep every TMA destination on a 1024-byte swizzle atom
-  if (G > 16 || lps < 3) return PKV_ERR_UNSUPPORTED;
+  const bool rows_path = lps < 3;
   if (pool->num_pages * (int64_t)pool->page_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   if (batch_size > 65535 || pool->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -670,7 +810,7 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   const int tpt = kBM / G;
   const uint64_t Hq = num_q_heads, Hkv = pool->num_kv_heads;
   const uint64_t rows = (uint64_t)pool->num_pages * pool->page_size;
-  const uint32_t R = pool->page_size < kBN ? pool->page_size : kBN;
+  const uint32_t R = rows_path ? 8 : (pool->page_size < kBN ? pool->page_size : kBN);  // TMA box rows
   const uint64_t Db = (uint64_t)D * 2;
   if (!pkv_host::encode_tmap_3d(&a.tm_q, q, D, Hq, (uint64_t)num_q_rows, Db, Hq * Db, 64, G, tpt) ||
       !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, D, Hkv, rows, Db, Hkv * Db, 64, 1, R) ||
@@ -686,6 +826,9 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   a.num_pages = pool->num_pages;
   a.page_size = pool->page_size;
   a.log2_ps = lps;
+  a.k_pool = (const __nv_bfloat16*)pool->k;
+  a.v_pool = (const __nv_bfloat16*)pool->v;
+  a.num_kv_heads = pool->num_kv_heads;
   a.num_q_heads = num_q_heads;
   a.group = G;
   a.rows_used = G * tpt;
@@ -711,8 +854,14 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   const int tiles = (max_rows + tpt - 1) / tpt;
   dim3 grid(tiles, pool->num_kv_heads, batch_size);
   cudaStream_t st = (cudaStream_t)stream;
-  if (D == 128) return causal ? launch_kernel<true, 128>(a, grid, st) : launch_kernel<false, 128>(a, grid, st);
-  return causal ? launch_kernel<true, 64>(a, grid, st) : launch_kernel<false, 64>(a, grid, st);
+  if (rows_path) {
+    if (D == 128)
+      return causal ? launch_kernel<true, 128, true>(a, grid, st) : launch_kernel<false, 128, true>(a, grid, st);
+    return causal ? launch_kernel<true, 64, true>(a, grid, st) : launch_kernel<false, 64, true>(a, grid, st);
+  }
+  if (D == 128)
+    return causal ? launch_kernel<true, 128, false>(a, grid, st) : launch_kernel<false, 128, false>(a, grid, st);
+  return causal ? launch_kernel<true, 64, false>(a, grid, st) : launch_kernel<false, 64, false>(a, grid, st);
 }
 
 }  // namespace

@@ -23,7 +23,7 @@ def _pool_batch(seed, ps, Hq, Hkv, lens, D=128):
 
 
 @pytest.mark.parametrize("ps,Hq,Hkv,D", [(16, 32, 8, 128), (8, 8, 8, 128), (64, 16, 2, 128), (32, 16, 16, 128),
-                                         (16, 14, 2, 64), (16, 12, 2, 128)])
+                                         (16, 14, 2, 64), (16, 12, 2, 128), (1, 16, 8, 128), (24, 14, 2, 64)])
 def test_shared_prefix_parts_match_oracle(lib, ps, Hq, Hkv, D):
     lens = (700, 64, 129, 1, 300, 2000)
     b = _pool_batch(90 + ps + Hq, ps, Hq, Hkv, lens, D)

@@ -122,6 +122,12 @@ GENERAL = [
     (16, 16, 16, 64, [(0, 129), (200, 64)]),                     # group 1, head_dim 64
     (64, 64, 4, 64, [(63, 17), (1, 8)]),                         # group 16, head_dim 64
     (16, 24, 2, 128, [(0, 30), (45, 11)]),                       # group 12: 120 rows
+    # page sizes the TMA boxes do not take (below 8 rows, or not a power of two): row copies
+    (1, 16, 8, 128, [(0, 40), (77, 13), (200, 64)]),             # page size 1 (Qwen3-0.6B shape)
+    (2, 14, 2, 64, [(5, 33), (0, 7)]),
+    (4, 32, 8, 128, [(63, 65), (128, 1), (0, 100)]),
+    (24, 8, 8, 128, [(47, 30), (0, 24), (100, 3)]),              # page size 24
+    (12, 6, 2, 64, [(11, 40), (36, 36)]),
 ]
 
 
@@ -184,14 +190,6 @@ def test_extend_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
     assert e.value.status == 2  # head_dim 96 not built
-    b = random_small_batch(21, page_size=24, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
-    with pytest.raises(lib.PagedKVError) as e:
-        run_extend(lib, b, b.k_pool, b.v_pool)
-    assert e.value.status == 2  # page size not a power of two
-    b = random_small_batch(23, page_size=4, num_q_heads=8, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
-    with pytest.raises(lib.PagedKVError) as e:
-        run_extend(lib, b, b.k_pool, b.v_pool)
-    assert e.value.status == 2  # pages smaller than 8 rows
     b = random_small_batch(22, page_size=16, num_q_heads=34, num_kv_heads=2, head_dim=128, extend=[(4, 4)])
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
