@@ -8,12 +8,14 @@
 // (nanoLLMServe README, "v0.7 Chunked Prefill") is the same call with a non-zero prefix.
 //
 // Design for GB300:
-//  * One CTA per (128-row Q tile, KV head, request).  The 128 rows are (token, group head) pairs:
-//    128/G consecutive tokens times the G query heads that share the KV head, so each K/V tile
-//    loaded is used by the whole group.  Q arrives by one 3-D TMA box per 64-column half.
+//  * One CTA per (128-row Q tile, KV head, request).  The rows are (token, group head) pairs:
+//    floor(128/G) consecutive tokens times the G query heads that share the KV head (G from 1
+//    to 16), so each K/V tile loaded is used by the whole group.  Q arrives by one 3-D TMA box
+//    per 64-column half (head_dim 64 or 128).
 //  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
-//    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle, into 2-stage rings filled by
-//    two producer warps (K with Q, and V), so the K stream runs ahead of the V stream.
+//    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle (other page sizes: row copies
+//    into the same layout), into 2-stage rings filled by two producer warps (K with Q, and V), so
+//    the K stream runs ahead of the V stream.
 //  * S = Q K^T (M=128, N=64, K=128) and O += P V (M=128, N=128, K=64) run as tcgen05.mma,
 //    accumulating in TMEM: S double-buffered (2 x 64 columns), O in 128 columns.  QK and PV are
 //    issued by two threads in different warps, each blocked in a try_wait on its own operands, so
@@ -26,7 +28,8 @@
 //    tile's columns.  The two halves of a row exchange partial maxima through shared memory, apply
 //    the causal mask and the online softmax in fp32 (the running max only moves when it grows by
 //    more than 2^8, so O is rescaled in TMEM rarely), and finally normalise their halves of the O
-//    row into a shared-memory tile that all eight warps copy out with coalesced stores.
+//    row (by the sum of the bf16-rounded probabilities the MMA used; the LSE takes the exact sum)
+//    into a shared-memory tile that all eight warps copy out with coalesced stores.
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include <atomic>
