@@ -106,3 +106,24 @@ def test_max_over_ranks_gloo_world2():
 
 def test_max_over_ranks_without_group():
     assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+
+
+def test_reference_arm_json_contract():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with the
+    contract's keys, for the workload asked for."""
+    import json
+    import subprocess
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--workload", "tiny"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["value"] > 0
+    assert line["config"]["workload"].startswith("tiny")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
