@@ -810,8 +810,10 @@ def main():
     ap.add_argument("--flush-l2", action="store_true",
                     help="zero a 256 MB buffer before every timed step (for workloads that fit in L2); "
                          "the step time is then the sum of the per-operation event times")
-    ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"])
-    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="all", choices=["all", "decode", "extend", "append"],
+                    help="time only one operation of the step (default: the whole step)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end run (host buffers, copies inside the timed region)")
     ap.add_argument("--rope", action="store_true",
                     help="fuse the rotary embedding of the new K and of all queries into the append")
     ap.add_argument("--eager", action="store_true",
@@ -821,12 +823,15 @@ def main():
                          "runs beside the decode in its own graph branch, else all)")
     ap.add_argument("--serial-step", action="store_true",
                     help="run the step's operations one after another on one stream (no branches)")
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of this node; N > 1 runs under torchrun, one replica per rank")
+    ap.add_argument("--steps", type=int, default=3000, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=10, help="untimed warm-up steps (at least 3)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"],
+                    help="reference: time the fp64 CPU oracle on the host cores instead")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="seconds of CPU-oracle work for the cpu_baseline figure")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the cpu_baseline figure")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads the CPU oracle may use (default: every affinity core)")
     args = ap.parse_args()
