@@ -30,4 +30,5 @@ from .attention import (  # noqa: F401
     rope_angles,
     rope,
     rope_kv_append,
+    bf16_round_nearest_even,
 )

@@ -356,11 +356,32 @@ def rope(x, positions, theta):
     return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
 
 
+def bf16_round_nearest_even(x):
+    """Round fp64 values once to the nearest bf16 value, ties to the even significand.
+
+    bf16 keeps 8 significant bits and fp32's exponent range: with x = m * 2**e (0.5 <= |m| < 1)
+    the neighbours are multiples of 2**(e - 8), or of 2**-133 below the smallest normal 2**-126.
+    ``np.round`` rounds halves to even.  Values past the largest finite bf16 become +-inf (the
+    result is returned in fp64, every element exactly a bf16 value).  Rounding straight from fp64
+    avoids the second rounding a cast through fp32 would add.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    step = np.maximum(e, -125) - 8  # exponent of the bf16 spacing at x
+    with np.errstate(over="ignore"):
+        y = np.ldexp(np.round(np.ldexp(x, -step)), step)
+        y = np.where(np.abs(y) >= 2.0 ** 128, np.copysign(np.inf, x), y)
+    return np.where(np.isfinite(x), y, x)
+
+
 def rope_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, positions, page_size, theta):
-    """KV write with RoPE applied to K: pool.k[slot[t]] = bf16(rope(k_new[t], pos[t])) (round to
-    nearest even from the fp64 rotation), pool.v[slot[t]] = v_new[t] bit-exact.  Negative slots
-    write nothing.  Returns (k_pool, v_pool, k_rot_f64) where k_rot_f64 is the unrounded rotation."""
+    """KV write with RoPE applied to K: pool.k[slot[t]] = bf16(rope(k_new[t], pos[t])), rounded
+    once to nearest even from the fp64 rotation; pool.v[slot[t]] = v_new[t] bit-exact.  Negative
+    slots write nothing.  Returns (k_pool, v_pool, k_rot_f64) where k_rot_f64 is the unrounded
+    rotation."""
     k_rot = rope(as_f64(k_new), _as_int(positions), theta)
-    k_bf16 = torch.tensor(k_rot).to(torch.bfloat16) if torch is not None else k_rot
+    k_r = bf16_round_nearest_even(k_rot)
+    # exact: every value of k_r is a bf16 value, so the casts through fp32 do not round
+    k_bf16 = torch.tensor(k_r).to(torch.float32).to(torch.bfloat16) if torch is not None else k_r
     kp, vp = kv_append(k_pool, v_pool, k_bf16, v_new, slot_mapping, page_size)
     return kp, vp, k_rot

@@ -6,12 +6,15 @@
   (torch scaled_dot_product_attention in fp64 with an explicit mask);
 - invariants (page relabelling, softmax rows summing to 1, split/merge = unsplit,
   decode = extend with one query);
-- a brute-force byte check of the KV append.
+- a brute-force byte check of the KV append, and of the RoPE append (pure-Python rotation per
+  token at its own position, bf16 rounding with exact rationals, V bit copies, padding skipped).
 The mutation tests at the end plant plausible mistakes in the oracle (on the
 CPU) and check that a pin catches each one.
 """
 
 import math
+import struct
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -488,3 +491,144 @@ def test_pin_catches_interleaved_rope(monkeypatch):
     c = GOLD["rope_quarter_turns"]
     out = oa.rope(np.array(c["x"], dtype=np.float64), c["positions"], c["theta"])
     assert np.abs(out - np.array(c["expect"])).max() > 0.1
+
+
+# ---------------------------------------------------------------------------
+# RoPE fused with the KV append: K rotated at its own position and rounded once to bf16, V copied,
+# padding skipped, nothing else touched
+# ---------------------------------------------------------------------------
+def _bf16_rne_bruteforce(x):
+    """The bf16 value nearest to x (ties to the even significand), found with exact rationals:
+    the two bf16 neighbours are consecutive multiples of the spacing at |x|, and the nearer one
+    wins.  Independent of the oracle's frexp/round formulation."""
+    if x == 0.0 or math.isnan(x) or math.isinf(x):
+        return x
+    _, e = math.frexp(abs(x))              # 2**(e-1) <= |x| < 2**e
+    ulp = Fraction(2) ** (max(e, -125) - 8)  # 8 significant bits; fixed spacing below 2**-126
+    fx = Fraction(x)
+    lo = (fx / ulp).__floor__()
+    below, above = fx - lo * ulp, (lo + 1) * ulp - fx
+    n = lo if below < above or (below == above and lo % 2 == 0) else lo + 1
+    y = float(n * ulp)
+    return math.copysign(math.inf, x) if abs(y) >= 2.0 ** 128 else y
+
+
+def _bits_of_bf16(v):
+    """bf16 bit pattern of a value that is exactly a bf16 value (the top half of its fp32 bits)."""
+    b = struct.unpack("<I", struct.pack("<f", v))[0]
+    assert b & 0xFFFF == 0
+    b >>= 16
+    return b - 0x10000 if b >= 0x8000 else b  # as int16, like torch's int16 view
+
+
+def _pin_rope_append(seed=41, theta=1.0e4):
+    """Check oracle.rope_kv_append against a byte-level brute force; returns the failures."""
+    b = _small(seed=seed)
+    T, Hkv, D, ps = b.num_new_tokens, b.num_kv_heads, b.head_dim, b.page_size
+    gen = torch.Generator().manual_seed(seed)
+    positions = torch.randint(0, 20000, (T,), generator=gen, dtype=torch.int32)
+    slots = b.slot_mapping.clone()
+    slots[2] = -1  # padding token
+    kp, vp, k_rot = oa.rope_kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, slots, positions, ps, theta)
+    fails = []
+    width = Hkv * D
+    before_k = b.k_pool.view(torch.int16).reshape(-1, width)
+    before_v = b.v_pool.view(torch.int16).reshape(-1, width)
+    after_k = kp.view(torch.int16).reshape(-1, width)
+    after_v = vp.view(torch.int16).reshape(-1, width)
+    new_v = b.v_new.view(torch.int16).reshape(T, width)
+    kx = b.k_new.float().double().numpy()
+    written = {}
+    for t, s in enumerate(slots.tolist()):
+        if s >= 0:
+            written[s] = t
+    for s in range(after_k.shape[0]):
+        t = written.get(s)
+        if t is None:  # padding or untouched slot: every byte as before (NaN rows by their bits)
+            if not (torch.equal(after_k[s], before_k[s]) and torch.equal(after_v[s], before_v[s])):
+                fails.append(f"slot {s} changed without a token")
+            continue
+        if not torch.equal(after_v[s], new_v[t]):
+            fails.append(f"V of token {t} is not a bit copy")
+        p = int(positions[t])
+        for h in range(Hkv):
+            rot = _rope_bruteforce(kx[t, h].tolist(), p, theta)
+            if np.abs(np.array(rot) - k_rot[t, h]).max() > 1e-12:
+                fails.append(f"rotation of token {t} head {h}")
+            want = [_bits_of_bf16(_bf16_rne_bruteforce(v)) for v in rot]
+            got = after_k[s, h * D:(h + 1) * D].tolist()
+            if got != want:
+                fails.append(f"K bits of token {t} head {h}")
+    return fails
+
+
+def test_rope_append_bruteforce_bytes():
+    assert _pin_rope_append() == []
+
+
+def test_bf16_rounding_ties_and_edges():
+    """Round-to-nearest-even cases fixed by the bf16 format itself (8 significant bits)."""
+    r = oracle.bf16_round_nearest_even
+    cases = {
+        1.0 + 2.0 ** -8: 1.0,                           # halfway, even neighbour below
+        1.0 + 3 * 2.0 ** -8: 1.0 + 2.0 ** -6,           # halfway, even neighbour above
+        1.0 + 2.0 ** -8 + 2.0 ** -40: 1.0 + 2.0 ** -7,  # just above halfway (a cast via fp32 gives 1.0)
+        -(1.0 + 2.0 ** -8 + 2.0 ** -40): -(1.0 + 2.0 ** -7),
+        2.0 ** -133: 2.0 ** -133,                       # smallest subnormal
+        3 * 2.0 ** -135: 2.0 ** -133,                   # 0.75 of it rounds up
+        (2.0 - 2.0 ** -7) * 2.0 ** 127: (2.0 - 2.0 ** -7) * 2.0 ** 127,  # largest finite
+        (2.0 - 2.0 ** -8) * 2.0 ** 127: math.inf,       # halfway to 2**128: overflows
+        0.0: 0.0,
+    }
+    got = r(np.array(list(cases)))
+    assert got.tolist() == list(cases.values())
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))
+    assert r(x).tolist() == [_bf16_rne_bruteforce(v) for v in x.tolist()]
+
+
+def test_pin_catches_rotated_v(monkeypatch):
+    orig = oa.rope_kv_append
+
+    def rotates_v(k_pool, v_pool, k_new, v_new, slot_mapping, positions, page_size, theta):
+        v_rot = oa.bf16_round_nearest_even(oa.rope(oa.as_f64(v_new), oa._as_int(positions), theta))
+        v_b = torch.tensor(v_rot).float().to(torch.bfloat16)
+        return orig(k_pool, v_pool, k_new, v_b, slot_mapping, positions, page_size, theta)
+
+    monkeypatch.setattr(oa, "rope_kv_append", rotates_v)
+    assert any("V of token" in f for f in _pin_rope_append())
+
+
+def test_pin_catches_token_index_as_position(monkeypatch):
+    orig = oa.rope_kv_append
+
+    def by_index(k_pool, v_pool, k_new, v_new, slot_mapping, positions, page_size, theta):
+        return orig(k_pool, v_pool, k_new, v_new, slot_mapping, np.arange(len(positions)), page_size, theta)
+
+    monkeypatch.setattr(oa, "rope_kv_append", by_index)
+    assert any("rotation of token" in f for f in _pin_rope_append())
+
+
+def test_pin_catches_truncation(monkeypatch):
+    def truncate(x):
+        x = np.asarray(x, dtype=np.float64)
+        m, e = np.frexp(x)
+        step = np.maximum(e, -125) - 8
+        return np.ldexp(np.trunc(np.ldexp(x, -step)), step)
+
+    monkeypatch.setattr(oa, "bf16_round_nearest_even", truncate)
+    fails = _pin_rope_append()
+    assert fails and all("K bits" in f for f in fails)
+
+
+def test_pin_catches_padding_written(monkeypatch):
+    orig = oa.kv_append
+
+    def no_skip(k_pool, v_pool, k_new, v_new, slot_mapping, page_size):
+        s = oa._as_int(slot_mapping).copy()
+        free = next(x for x in range(k_pool.shape[0] * page_size) if x not in set(s.tolist()))
+        s[s < 0] = free  # a padding token written into a slot no token owns
+        return orig(k_pool, v_pool, k_new, v_new, s, page_size)
+
+    monkeypatch.setattr(oa, "kv_append", no_skip)
+    assert any("changed without a token" in f or "V of token" in f for f in _pin_rope_append())
