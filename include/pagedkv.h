@@ -26,7 +26,10 @@
  *
  * Calls are asynchronous on the given stream (a cudaStream_t passed as void*, NULL = legacy
  * default stream), never synchronise the host and never allocate: every scratch buffer
- * ("workspace") is passed in by the caller, so a call can be captured in a CUDA graph.
+ * ("workspace") is passed in by the caller, so a call can be captured in a CUDA graph.  The one
+ * exception is pkv_paged_decode_noalloc, which keeps its scratch in an array the library holds on
+ * each device; its own comment gives the rules for that array (shared by all its calls, first
+ * call on a device before any stream capture).
  *
  * Errors: arguments that can be checked on the host (null pointers, shapes, alignment,
  * workspace size) return a status and launch nothing.  Kernels bounds-check every page index
@@ -56,7 +59,9 @@ typedef enum {
 /* Bits OR-ed into *err_word by kernels. */
 #define PKV_DEVERR_PAGE_OOB 0x1u /* a page index outside [0, num_pages) was skipped */
 #define PKV_DEVERR_SLOT_OOB 0x2u /* an append slot >= num_pages * page_size was skipped */
-#define PKV_DEVERR_LENGTH 0x4u   /* a KV length exceeds the request's pages, or a decode length is 0 */
+#define PKV_DEVERR_LENGTH 0x4u   /* a KV length exceeds the request's pages, a decode length is 0,
+                                    or an extend / shared-prefix part has more query rows than
+                                    max_extend_len / max_part_rows covers (or a negative count) */
 #define PKV_DEVERR_TIMEOUT 0x8u  /* a bounded in-kernel wait gave up */
 #define PKV_DEVERR_INTERNAL 0x10u /* a launch-time invariant failed and the CTA skipped its work */
 #define PKV_DEVERR_ROW_OOB 0x20u   /* a query or output row range outside q / out was skipped */
@@ -206,7 +211,9 @@ pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t ba
  *   - Shapes whose pkv_decode_workspace_size() exceeds PKV_DECODE_NOALLOC_SCRATCH_BYTES are
  *     rejected with PKV_ERR_WORKSPACE (Hq=32, head_dim 128 fits about 800 requests).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, which
- *     may load the module on that device); make that first call before any stream capture.
+ *     may load the module on that device); make that first call before any stream capture.  A
+ *     device reset (cudaDeviceReset) frees the array with its context: the next call on that
+ *     device looks the address up again and, like a first call, must come before any capture.
  *   - Every call shares the one array and it keeps the last call's contents; nothing in it needs
  *     to start at zero.  Calls that can overlap on the GPU (different streams without ordering)
  *     race on it: serialise them.
@@ -236,8 +243,9 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
  *   q          bf16 [num_q_tokens, num_q_heads, head_dim] (device)
  *   num_q_tokens  rows of q and out (= qo_indptr[batch_size])
  *   qo_indptr  int32 [batch_size+1]; prefix_lens int32 [batch_size] (device)
- *   max_extend_len  an upper bound of qo_indptr[b+1]-qo_indptr[b] over b (sizes the grid;
- *              rows beyond it are not computed)
+ *   max_extend_len  an upper bound of qo_indptr[b+1]-qo_indptr[b] over b (sizes the grid).
+ *              A request with more rows than the grid covers, or with qo_indptr decreasing,
+ *              reports PKV_DEVERR_LENGTH and its rows past the grid are left unwritten.
  *   out        bf16 [num_q_tokens, num_q_heads, head_dim]; lse nullable fp32 [num_q_tokens, num_q_heads]
  *   workspace  device, 16-byte aligned, at least pkv_extend_workspace_size(...) bytes, caller-owned
  *              and not shared with a call in flight on another stream (may be NULL when that
@@ -274,7 +282,8 @@ size_t pkv_shared_prefix_workspace_size(int32_t num_parts, int32_t num_q_heads, 
  * A part with kv_lens[p] == 0 writes o = 0 and lse = -inf (an empty split for the merge).
  *   q          bf16 [num_q_rows, num_q_heads, head_dim] (device)
  *   q_start, q_len, o_start, kv_lens  int32 [num_parts]; kv_indptr int32 [num_parts+1] (device)
- *   max_part_rows  an upper bound of q_len[p] (sizes the grid; rows beyond it are not computed)
+ *   max_part_rows  an upper bound of q_len[p] (sizes the grid); a longer or negative part reports
+ *              PKV_DEVERR_LENGTH and its rows past the grid are left unwritten
  *   o_part     bf16 [num_out_rows, num_q_heads, head_dim]; lse_part nullable fp32 [num_out_rows, num_q_heads]
  *   workspace  as for pkv_paged_extend, pkv_shared_prefix_workspace_size(...) bytes
  *   err_word   nullable; PKV_DEVERR_ROW_OOB for a part whose rows fall outside q or o_part (the part

@@ -63,6 +63,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+void* driver_entry(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return p;
+}
+}  // namespace
+
+unsigned long long current_context_id() {
+  static std::atomic<CtxGetCurrentFn> get_cur{nullptr};
+  static std::atomic<CtxGetIdFn> get_id{nullptr};
+  CtxGetCurrentFn fc = get_cur.load();
+  CtxGetIdFn fi = get_id.load();
+  if (!fc || !fi) {
+    fc = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent", 4000));
+    fi = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId", 12000));
+    if (!fc || !fi) return 0;
+    get_cur.store(fc);
+    get_id.store(fi);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fc(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (fi(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 bool encode_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                     uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
   auto fn = encode_fn();

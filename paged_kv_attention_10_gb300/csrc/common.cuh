@@ -215,4 +215,7 @@ int current_device();
 bool aligned16(const void* p);
 pkv_status launch_status();         // PKV_OK or PKV_ERR_CUDA after a launch
 bool valid_pool(const pkv_pool* p); // non-null, positive sizes, aligned
+// Process-unique id of the calling thread's current CUDA context (cuCtxGetId), 0 when there is
+// none or it cannot be read.  A context created after a device reset gets a new id.
+unsigned long long current_context_id();
 }  // namespace pkv_host

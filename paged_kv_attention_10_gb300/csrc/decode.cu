@@ -147,7 +147,9 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
     return k < 32 ? v0 : v1;
   };
 
+  int nissued = 0;  // stages handed to the consumers (copies, or the end marker)
   auto next_stage = [&]() {
+    ++nissued;
     if (++stage == NS) {
       stage = 0;
       phase ^= 1;
@@ -321,6 +323,16 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
     }
   }
   if (ok) emit(-1, 0, 0, 0, 0, 0);
+  // Wait (bounded) until the copies of the last NS stages issued have landed, so that no copy
+  // into this CTA's shared memory is in flight when it exits, also when the consumers gave up on
+  // a wait and left.  On the normal path the consumers have already seen every stage complete.
+  for (int k = 0; k < min(nissued, NS); ++k) {
+    if (--stage < 0) {
+      stage = NS - 1;
+      phase ^= 1;
+    }
+    mbar_wait(&full[stage], phase);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1059,20 +1071,25 @@ static __device__ __align__(256) uint8_t g_decode_scratch[PKV_DECODE_NOALLOC_SCR
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[64] = {nullptr};
+unsigned long long g_scratch_ctx[64] = {0};  // context the cached address belongs to
 
-// Device address of g_decode_scratch on the current device (looked up once per device; in host
-// code the array's name is only a stand-in for the symbol, never a device pointer).
+// Device address of g_decode_scratch on the current device (in host code the array's name is
+// only a stand-in for the symbol, never a device pointer).  Looked up once per device, and again
+// when the device's context has changed (after a cudaDeviceReset the old address is gone).
 void* scratch_on_current_device() {
   const int dev = pkv_host::current_device();
   if (dev < 0 || dev >= 64) return nullptr;
+  const unsigned long long ctx = pkv_host::current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) {
       cudaGetLastError();
       return nullptr;
     }
     g_scratch_addr[dev] = p;
+    // the lookup creates the context if there was none yet
+    g_scratch_ctx[dev] = ctx != 0 ? ctx : pkv_host::current_context_id();
   }
   return g_scratch_addr[dev];
 }

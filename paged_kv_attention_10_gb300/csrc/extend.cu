@@ -595,6 +595,12 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     w.qo0 = __ldg(a.o_start + w.b);
     w.E = __ldg(a.q_len + w.b);
   }
+  // the grid covers gridDim.x * tokens_per_tile rows of each request (max_extend_len, or the
+  // largest part): a request with more rows, or a negative count, is reported once, by the CTA
+  // of its first tile, and its rows past the grid stay unwritten
+  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == 0 && threadIdx.x == 0 &&
+      (w.E < 0 || w.E > (int)gridDim.x * a.tokens_per_tile))
+    report(a.err_word, PKV_DEVERR_LENGTH);
   if (w.t0 >= w.E) return;  // uniform: this tile has no rows
   if (w.q0 < 0 || w.qo0 < 0 || w.q0 > a.num_q_rows - w.E || w.qo0 > a.num_out_rows - w.E) {
     if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_ROW_OOB);

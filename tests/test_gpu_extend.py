@@ -185,6 +185,31 @@ def test_extend_bad_page_index_is_reported(lib):
     assert int(err.item()) & lib.DEVERR_PAGE_OOB
 
 
+def test_extend_rows_past_max_extend_len_are_reported(lib):
+    """A max_extend_len below a request's new-token count is a caller error the kernel reports:
+    PKV_DEVERR_LENGTH, the rows the grid covers computed, the rows past it left untouched."""
+    b = random_small_batch(27, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                           extend=[(0, 300), (50, 70)])
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(b.ext_q, 7.0).cuda()
+    too_small = 100  # group 4: the grid covers ceil(100 / 32) * 32 = 128 rows of each request
+    lib.paged_extend(b.ext_q.cuda(), kp.cuda(), vp.cuda(), b.ext_qo_indptr.cuda(), b.ext_kv_indptr.cuda(),
+                     b.ext_kv_indices.cuda(), b.ext_prefix_lens.cuda(), too_small, b.sm_scale, out=out,
+                     err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == lib.DEVERR_LENGTH
+    o_ref, _ = oracle_extend(b, kp, vp)
+    covered = list(range(0, 128)) + list(range(300, 370))
+    assert_attention_close(out, None, o_ref, None, rows=covered, what="covered rows")
+    assert bool((out[128:300].float() == 7.0).all())
+    # with a large enough bound the same call reports nothing
+    err.zero_()
+    run_extend(lib, b, kp, vp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
 def test_extend_host_checks(lib):
     b = random_small_batch(20, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=96, extend=[(4, 4)])
     with pytest.raises(lib.PagedKVError) as e:

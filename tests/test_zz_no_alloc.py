@@ -4,7 +4,7 @@ pkv_paged_decode_noalloc serves callers that cannot allocate device memory when 
 engine whose KV pool was given a fixed share of HBM up front, or code that must not take
 cudaMalloc's implicit synchronisation mid-step): it keeps its split partials in a scratch array the
 library holds in device memory.  Its results must equal those of pkv_paged_decode with a
-caller-supplied workspace, on consecutive calls that reuse the same scratch.
+caller-supplied workspace and the fp64 oracle's, on consecutive calls that reuse the same scratch.
 
 This file is named to be collected last, so a run that stops at the first failure has already run
 every other test; it also passes on its own in a fresh process.
@@ -14,6 +14,7 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import pytest
 import torch
 
@@ -66,36 +67,47 @@ def _p(x):
 
 
 def _decode_pair(cdll, b, t, pool):
-    """(out, lse) from the workspace entry point and from the no-alloc entry point."""
+    """(out, lse) from the workspace entry point and from the no-alloc entry point, and the two
+    calls' device error words (both start at zero)."""
     B, hq = b.num_decode, b.num_q_heads
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     ws_bytes = cdll.pkv_decode_workspace_size(B, hq, b.num_kv_heads, b.head_dim)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
     out_ref = torch.empty_like(t["q"])
     lse_ref = torch.empty((B, hq), dtype=torch.float32, device="cuda")
     st = cdll.pkv_paged_decode(ctypes.byref(pool), _p(t["q"]), B, hq, _p(t["ind"]), _p(t["idx"]),
                                _p(t["lens"]), b.sm_scale, _p(out_ref), _p(lse_ref), _p(ws), ws_bytes,
-                               None, stream)
+                               _p(err[0:1]), stream)
     assert st == 0
     out = torch.full_like(t["q"], float("nan"))
     lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device="cuda")
     st = cdll.pkv_paged_decode_noalloc(ctypes.byref(pool), _p(t["q"]), B, hq, _p(t["ind"]),
-                                       _p(t["idx"]), _p(t["lens"]), b.sm_scale, _p(out), _p(lse), None,
-                                       stream)
+                                       _p(t["idx"]), _p(t["lens"]), b.sm_scale, _p(out), _p(lse),
+                                       _p(err[1:2]), stream)
     assert st == 0
     torch.cuda.synchronize()
-    return out_ref, lse_ref, out, lse
+    return out_ref, lse_ref, out, lse, err.cpu().tolist()
 
 
 def test_noalloc_decode_matches_workspace_decode_twice(cdll):
     # two calls in a row: long split requests first, then a different batch that reuses the
-    # scratch the first call left behind
+    # scratch the first call left behind.  Each is checked against the workspace decode and
+    # against the fp64 oracle, and neither call may raise a device error bit (a merge that read a
+    # stale entry of the reused scratch would show up in the output or in the error word).
     for seed, lens in ((41, (3000, 17, 9000, 1, 640, 2049)), (42, (5, 700, 33, 4096, 128))):
         b, t, pool = _device_batch(seed, lens)
-        out_ref, lse_ref, out, lse = _decode_pair(cdll, b, t, pool)
+        out_ref, lse_ref, out, lse, err = _decode_pair(cdll, b, t, pool)
+        assert err == [0, 0]
         d = (out.float() - out_ref.float()).abs()
         assert d.max().item() <= O_MAX_ABS and d.mean().item() <= O_MEAN_ABS
         assert (lse - lse_ref).abs().max().item() <= LSE_ABS
+        kp, vp = t["kp"].cpu(), t["vp"].cpu()
+        o_or, lse_or = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices,
+                                           b.dec_kv_lens, b.page_size, b.sm_scale)
+        do = np.abs(out.float().cpu().numpy().astype(np.float64) - o_or)
+        assert do.max() <= O_MAX_ABS and do.mean() <= O_MEAN_ABS, (do.max(), do.mean())
+        assert np.abs(lse.cpu().numpy().astype(np.float64) - lse_or).max() <= LSE_ABS
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(cdll):
