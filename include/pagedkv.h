@@ -147,6 +147,17 @@ pkv_status pkv_rope_kv_append(const pkv_pool* pool, const void* k_new, const voi
                               void* stream);
 
 /*
+ * The cos/sin table pkv_rope_kv_append reads, computed on the device.  Row p of
+ * table fp32 [max_position, head_dim] (device, caller-owned) receives cos(a_i) in columns
+ * [0, D/2) and sin(a_i) in [D/2, D), a_i = p * theta^(-2i/D) (the half-split rotary embedding of
+ * HF Llama/Qwen checkpoints, nanoSGLang README "Notable Fixes").  The angle is formed in double
+ * precision and cos/sin are rounded once to fp32.  head_dim even, theta > 0 (e.g. 1e4 for
+ * Llama, 1e6 for Qwen3), max_position >= 0 (0 launches nothing).  Asynchronous on the stream.
+ */
+pkv_status pkv_rope_cos_sin_table(float* table, int32_t max_position, int32_t head_dim, double theta,
+                                  void* stream);
+
+/*
  * Page gather (test and debug op): copy every request's K and V rows, in position order, into
  * contiguous buffers.  Request b occupies rows [sum_{b'<b} kv_lens[b'], ... + kv_lens[b]).
  *   kv_indptr  int32 [batch_size+1], kv_indices int32 [kv_indptr[batch_size]], kv_lens int32
@@ -299,6 +310,61 @@ pkv_status pkv_shared_prefix_attention(const pkv_pool* pool, const void* q, int3
                                        void* o_part, float* lse_part, int32_t num_out_rows,
                                        void* workspace, size_t workspace_bytes, uint32_t* err_word,
                                        void* stream);
+
+/*
+ * Host plan of a shared-prefix (cascade) decode: the integer arrays pkv_shared_prefix_attention,
+ * pkv_paged_decode and pkv_merge_states_bf16 take, computed on the CPU from HOST copies of the
+ * decode batch's page lists (the "plan" of a plan/run split: mini-sglang from Scratch handbook,
+ * "What you will be able to do").  No attention arithmetic happens here.
+ *
+ * Groups g < num_groups are runs of consecutive requests [group_first[g], + group_count[g]) that
+ * share leading pages (radix-cache prefixes).  A group's shared length is the longest common
+ * leading run of page ids of its members, cut so that every member keeps at least one position
+ * of its own; shared_tokens[g] (nullable, [num_groups]) receives it in positions, 0 for a group
+ * that shares nothing (then treated as unshared).  The shared pages of every group are cut into
+ * the same number S of chunks (sizes->num_splits): as many as one wave of CTAs covers
+ * (num_sms * ctas_per_sm over num_kv_heads * ceil(members / (128 / group_size)) CTAs per chunk),
+ * and no chunk shorter than min_chunk_tokens.
+ *
+ * Partial states are laid out as splits of one buffer [S + 1, batch_size, Hq, ...]: split s < S
+ * of row r is chunk s of r's group (an empty state for rows outside every group and chunks a
+ * group does not have), split S is the decode over r's own pages.
+ *   part p (p < num_parts):  query rows part_q_start[p] .. + part_q_len[p]; output rows
+ *     part_o_start[p] = s * batch_size + part_q_start[p]; page list part_kv_indices
+ *     [part_kv_indptr[p] .. part_kv_indptr[p+1]) with part_kv_lens[p] = its pages * page_size
+ *     (0 for an empty state)
+ *   own pages of request r:  suffix_kv_indices[suffix_kv_indptr[r] .. suffix_kv_indptr[r+1]),
+ *     suffix_kv_lens[r] >= 1 positions
+ * Inputs (host): kv_indptr int32 [batch_size+1] (kv_indptr[0] == 0, non-decreasing), kv_indices
+ * int32 [kv_indptr[batch_size]], kv_lens int32 [batch_size].  group_size = Hq / Hkv in 1..16.
+ * Outputs (host, caller-owned): sizes (required) receives the counts.  With every output array
+ * NULL the call only fills sizes (a size query).  Otherwise all nine arrays are required:
+ * part_* of parts_capacity entries (part_kv_indptr one more), part_kv_indices and
+ * suffix_kv_indices of indices_capacity entries (kv_indptr[batch_size] always suffices),
+ * suffix_kv_indptr [batch_size+1], suffix_kv_lens [batch_size]; too small a capacity returns
+ * PKV_ERR_WORKSPACE with sizes filled.  Groups outside the batch or overlapping, and bad counts,
+ * return PKV_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int32_t num_splits;         /* S: shared-prefix chunks; the own-pages decode is split S */
+  int32_t num_parts;          /* parts of pkv_shared_prefix_attention */
+  int32_t max_part_rows;      /* the largest part_q_len (its max_part_rows argument) */
+  int32_t num_part_indices;   /* entries written to part_kv_indices */
+  int32_t num_suffix_indices; /* entries written to suffix_kv_indices */
+} pkv_cascade_sizes;
+
+pkv_status pkv_plan_shared_prefix(const int32_t* kv_indptr, const int32_t* kv_indices,
+                                  const int32_t* kv_lens, int32_t batch_size,
+                                  const int32_t* group_first, const int32_t* group_count,
+                                  int32_t num_groups, int32_t page_size, int32_t num_kv_heads,
+                                  int32_t group_size, int32_t num_sms, int32_t ctas_per_sm,
+                                  int32_t min_chunk_tokens, pkv_cascade_sizes* sizes,
+                                  int32_t* shared_tokens, int32_t* part_q_start, int32_t* part_q_len,
+                                  int32_t* part_o_start, int32_t* part_kv_indptr,
+                                  int32_t* part_kv_indices, int32_t* part_kv_lens,
+                                  int32_t* suffix_kv_indptr, int32_t* suffix_kv_indices,
+                                  int32_t* suffix_kv_lens, int32_t parts_capacity,
+                                  int32_t indices_capacity);
 
 /*
  * Log-sum-exp merge of split partial states (flash-decoding).  For each row n and head h:

@@ -45,6 +45,11 @@ class Pool(ctypes.Structure):
                 ("num_kv_heads", _c_i32), ("head_dim", _c_i32)]
 
 
+class CascadeSizes(ctypes.Structure):
+    _fields_ = [("num_splits", _c_i32), ("num_parts", _c_i32), ("max_part_rows", _c_i32),
+                ("num_part_indices", _c_i32), ("num_suffix_indices", _c_i32)]
+
+
 class PagedKVError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
@@ -89,6 +94,11 @@ def load():
         "pkv_selftest_bounded_wait": (_c_i32, [_vp, _vp]),
         "pkv_validate_page_table": (_c_i32, [_vp, _vp, _vp, _c_i32, _c_i64, _c_i32, _c_i32, _vp]),
         "pkv_validate_slots": (_c_i32, [_vp, _c_i32, _c_i64, _vp]),
+        "pkv_rope_cos_sin_table": (_c_i32, [_vp, _c_i32, _c_i32, ctypes.c_double, _vp]),
+        "pkv_plan_shared_prefix": (_c_i32, [_vp, _vp, _vp, _c_i32, _vp, _vp, _c_i32, _c_i32, _c_i32,
+                                            _c_i32, _c_i32, _c_i32, _c_i32, ctypes.POINTER(CascadeSizes),
+                                            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_i32,
+                                            _c_i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -214,15 +224,21 @@ def kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stream=
               _ptr(err_word), _stream_ptr(stream, dev))
 
 
-def rope_cos_sin_table(max_position: int, head_dim: int, theta: float, device=None) -> torch.Tensor:
-    """The fp32 [max_position, head_dim] cos/sin table rope_kv_append reads: row p holds
-    cos(p * theta^(-2i/D)) for i < D/2, then the sines.  Built once, in fp64 on the host (large
-    positions keep full angle accuracy), like a model's rotary buffer."""
-    i = torch.arange(head_dim // 2, dtype=torch.float64)
-    inv_freq = theta ** (-2.0 * i / head_dim)
-    ang = torch.arange(max_position, dtype=torch.float64)[:, None] * inv_freq[None, :]
-    t = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
-    return t.to(device) if device is not None else t
+def rope_cos_sin_table(max_position: int, head_dim: int, theta: float, device=None, out=None,
+                       stream=None) -> torch.Tensor:
+    """The fp32 [max_position, head_dim] cos/sin table rope_kv_append reads (row p: cos of the
+    angles p * theta^(-2i/D), then their sines), computed by the library on ``device`` (default:
+    the current CUDA device).  Built once, like a model's rotary buffer."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty((max_position, head_dim), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    if out.shape != (max_position, head_dim):
+        raise ValueError("out must be [max_position, head_dim]")
+    with torch.cuda.device(dev):
+        _call("pkv_rope_cos_sin_table", _ptr(out), int(max_position), int(head_dim), float(theta),
+              _stream_ptr(stream, dev))
+    return out
 
 
 def rope_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, positions, cos_sin, q=None,

@@ -120,3 +120,48 @@ extern "C" pkv_status pkv_rope_kv_append(const pkv_pool* pool, const void* k_new
       pool->num_pages * pool->page_size, err_word);
   return pkv_host::launch_status();
 }
+
+// ---------------------------------------------------------------------------------------------
+// The cos/sin table the fused append reads.  Row p, column i < D/2: cos(a), column D/2 + i:
+// sin(a), with the angle a = p * theta^(-2i/D) of pair i at position p (the half-split rotary
+// embedding of HF Llama/Qwen checkpoints, nanoSGLang README "Notable Fixes").  The angle is
+// formed in double precision, so that large positions keep it to well under an fp32 ulp of the
+// cosine, and cos/sin come from CUDA's double-precision sincos before the fp32 rounding.  Built
+// once, like a model's rotary buffer; the double-precision work (~2M angles for 32K positions of
+// D = 128) takes well under a millisecond.
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+__global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ table, int32_t max_position,
+                                                        int32_t head_dim, double theta) {
+  const int half = head_dim / 2;
+  const int64_t n = (int64_t)max_position * half;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t p = idx / half;
+    const int i = (int)(idx - p * half);
+    const double inv_freq = pow(theta, -2.0 * (double)i / (double)head_dim);
+    double s, c;
+    sincos((double)p * inv_freq, &s, &c);
+    table[p * head_dim + i] = (float)c;
+    table[p * head_dim + half + i] = (float)s;
+  }
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_rope_cos_sin_table(float* table, int32_t max_position, int32_t head_dim,
+                                             double theta, void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_rope_cos_sin_table");
+  if (max_position < 0 || head_dim <= 0 || head_dim % 2 != 0 || !(theta > 0.0)) return PKV_ERR_INVALID_ARG;
+  if (max_position == 0) return PKV_OK;
+  if (!table) return PKV_ERR_INVALID_ARG;
+  const int64_t n = (int64_t)max_position * (head_dim / 2);
+  const int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  const int64_t cap = (int64_t)pkv_host::sm_count() * 8;
+  if (cap > 0 && blocks > cap) blocks = cap;
+  rope_table_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(table, max_position, head_dim,
+                                                                            theta);
+  return pkv_host::launch_status();
+}

@@ -33,7 +33,8 @@ def test_header_declares_the_hot_path():
     for n in ("pkv_kv_append", "pkv_paged_gather", "pkv_paged_decode", "pkv_paged_extend",
               "pkv_merge_states", "pkv_decode_workspace_size", "pkv_extend_workspace_size",
               "pkv_status_string", "pkv_version", "pkv_shared_prefix_attention",
-              "pkv_shared_prefix_workspace_size", "pkv_merge_states_bf16"):
+              "pkv_shared_prefix_workspace_size", "pkv_merge_states_bf16", "pkv_rope_cos_sin_table",
+              "pkv_plan_shared_prefix"):
         assert n in names
 
 

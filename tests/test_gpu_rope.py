@@ -32,11 +32,14 @@ def _positions(b, gen):
     return torch.randint(0, 32768, (b.num_new_tokens,), generator=gen, dtype=torch.int32)
 
 
-def test_table_matches_oracle_angles(lib):
-    t = lib.rope_cos_sin_table(100, 128, THETA)
-    ang = oracle.rope_angles(np.arange(100), 128, THETA)
-    assert np.abs(t[:, :64].double().numpy() - np.cos(ang)).max() < 1e-7
-    assert np.abs(t[:, 64:].double().numpy() - np.sin(ang)).max() < 1e-7
+@pytest.mark.parametrize("npos,D,theta", [(100, 128, THETA), (32768, 128, THETA), (4096, 64, 1.0e4)])
+def test_table_matches_oracle_angles(lib, npos, D, theta):
+    # the library builds the table on the device from double-precision angles; each entry is
+    # within an fp32 rounding (2^-25 of a value at most 1) of the fp64 cos/sin
+    t = lib.rope_cos_sin_table(npos, D, theta).cpu()
+    ang = oracle.rope_angles(np.arange(npos), D, theta)
+    assert np.abs(t[:, : D // 2].double().numpy() - np.cos(ang)).max() < 1e-7
+    assert np.abs(t[:, D // 2:].double().numpy() - np.sin(ang)).max() < 1e-7
 
 
 @pytest.mark.parametrize("hkv,hq,D", [(8, 32, 128), (2, 14, 64)])
