@@ -229,7 +229,9 @@ def rope_cos_sin_table(max_position: int, head_dim: int, theta: float, device=No
     """The fp32 [max_position, head_dim] cos/sin table rope_kv_append reads (row p: cos of the
     angles p * theta^(-2i/D), then their sines), computed by the library on ``device`` (default:
     the current CUDA device).  Built once, like a model's rotary buffer."""
-    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = torch.empty((max_position, head_dim), dtype=torch.float32, device=dev)
     _need(out, "out", torch.float32, dev)

@@ -24,12 +24,14 @@
 //    one N=128 MMA per 16 positions rather than two of N=64.
 //    P is written back as bf16 pairs over the S columns it came from and the PV MMA reads it from
 //    TMEM, so P never passes through shared memory.
-//  * Eight softmax warps, two per TMEM lane quadrant: a thread owns one row and one half of the
-//    tile's columns.  The two halves of a row exchange partial maxima through shared memory, apply
-//    the causal mask and the online softmax in fp32 (the running max only moves when it grows by
-//    more than 2^8, so O is rescaled in TMEM rarely), and finally normalise their halves of the O
-//    row (by the sum of the bf16-rounded probabilities the MMA used; the LSE takes the exact sum)
-//    into a shared-memory tile that all eight warps copy out with coalesced stores.
+//  * Four softmax warps, one per TMEM lane quadrant: a thread owns one row of the tile and reads
+//    all 64 of its scores, so the row max needs no exchange between warps (a three-input max.f32
+//    folds three scores per instruction).  It applies the causal mask and the online softmax in
+//    fp32 (the running max only moves when it grows by more than 2^8, so O is rescaled in TMEM
+//    rarely), keeps two sums of the probabilities (the exact one for the LSE; the one of the bf16
+//    values the PV MMA uses, accumulated straight from the packed bf16 pairs by the sm_100
+//    family's mixed-precision add, for O), and finally normalises its O row into a shared-memory
+//    tile that the four warps copy out with coalesced stores.
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include <atomic>
@@ -42,9 +44,12 @@ using namespace pkv;
 
 constexpr int kBM = 128;  // Q tile rows: (token, group head) pairs
 constexpr int kBN = 64;   // KV positions per tile
-// warp 0 Q/K loads, warp 1 QK MMAs, warps 2..9 softmax, warp 10 V loads, warp 11 PV MMAs
-constexpr int kThreads = 384;
-constexpr int kSoftmaxWarps = 8;
+// warp 0 Q/K loads, warp 1 QK MMAs, warps 2..5 softmax (one per TMEM lane quadrant, a thread
+// per row of the tile), warp 6 V loads, warp 7 PV MMAs
+constexpr int kSoftmaxWarps = 4;
+constexpr int kVWarp = 2 + kSoftmaxWarps;
+constexpr int kPVWarp = kVWarp + 1;
+constexpr int kThreads = (kPVWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;  // O at TMEM columns [128, 128 + D); S buffers at [0,64) and [64,128)
 constexpr uint32_t kQHalf = kBM * 128;   // one 64-dim half of the Q tile, 16 KB
@@ -60,9 +65,7 @@ struct Cfg {
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
-  static constexpr uint32_t kOffX = kOffV + 2 * kKVStage;   // row-max exchange [tile parity][half][row]
-  static constexpr uint32_t kOffL = kOffX + 2 * 2 * kBM * 4;  // row-sum exchange [sum][half][row]
-  static constexpr uint32_t kOffBar = kOffL + 2 * 2 * kBM * 4;
+  static constexpr uint32_t kOffBar = kOffV + 2 * kKVStage;
   static constexpr uint32_t kSmemBytes = kOffBar + 256;
   static constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of an O row
 };
@@ -366,38 +369,52 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
-template <int N>
-__device__ __forceinline__ float tree_max(float (&v)[N]) {
-#pragma unroll
-  for (int w = N / 2; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) v[i] = fmaxf(v[i], v[i + w]);
-  return v[0];
+// acc + (float)(low or high bf16 half of v), one rounding: the sm_100 family's mixed-precision add
+__device__ __forceinline__ float add_bf16_lo(uint32_t v, float acc) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(r) : "r"(v), "f"(acc));
+  return r;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t v, float acc) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(r) : "r"(v), "f"(acc));
+  return r;
 }
 
-// barrier of all eight softmax warps (id 5)
+// max of three (the sm_100 family's three-input max.f32)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max of 32 values in 16 three-input maxima: 32 -> 11 -> 4 -> 1
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = fmaxf(v[30], v[31]);
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
+  const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return fmaxf(max3f(b0, b1, b2), b3);
+}
+
+// barrier of all softmax warps (id 5)
 __device__ __forceinline__ void softmax_bar() {
-  asm volatile("bar.sync 5, 256;" ::: "memory");
+  asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
 }
 
-// barrier shared by the two softmax warps of TMEM lane quadrant wq (ids 1..4)
-__device__ __forceinline__ void pair_bar(int wq) {
-  switch (wq) {
-    case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
-    case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
-    case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
-    default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
-  }
-}
-
+// Softmax with one thread per row of the tile (four warps, one per TMEM lane quadrant): the
+// thread reads all 64 scores of its row, so the row max needs no exchange between warps.
 template <int D>
 __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, uint32_t tmem,
                                const Work& w) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp & 3;            // TMEM lane quadrant this warp may access
-  const int hsel = (warp - 2) >> 2;   // which half of the tile's columns this warp owns
-  const int r = wq * 32 + lane;       // tile row == TMEM lane
+  const int wq = warp & 3;       // TMEM lane quadrant this warp may access
+  const int r = wq * 32 + lane;  // tile row == TMEM lane
   const int tid = (warp - 2) * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
   const int G = a.group;
@@ -407,13 +424,10 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   const bool valid = r < a.rows_used && tok < w.E;
   const int limit = min(w.mask0 + tok, w.L - 1);        // last visible KV position of this row
   const int min_limit = min(w.mask0 + w.t0, w.L - 1);  // smallest limit over the tile's rows
-  // scores are scaled inside one FFMA, x = s * scale - m * scale; with a non-positive scale the
-  // max of s is not the max of the scaled scores, so scale first
   const bool pos_scale = a.scale_log2 > 0.f;
   const float sc = pos_scale ? a.scale_log2 : 1.f;
-  float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
   float m_used = -INFINITY;  // running max of the scaled (log2) scores
-  float l = 0.f;             // this half's running sum of the probabilities (for the LSE)
+  float l = 0.f;             // running sum of the probabilities (for the LSE)
   float lr = 0.f;            // ... of the probabilities as rounded to bf16 for the PV MMA (for O)
   bool ok = true;
 
@@ -422,87 +436,84 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[st], (j >> 1) & 1));
     if (!ok) break;
     tc_fence_after();
-    float sm[32];  // this half's scores of the row
-    tmem_ld32(taddr + st * 64 + hsel * 32, sm);
+    float s0[32], s1[32];  // the row's scores, positions [0, 32) and [32, 64) of the tile
+    tmem_ld32(taddr + st * 64, s0);
+    tmem_ld32(taddr + st * 64 + 32, s1);
     tmem_wait_ld();
-
     const int pos0 = j * kBN;
     if (!pos_scale) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sm[c] *= a.scale_log2;
+      for (int c = 0; c < 32; ++c) {
+        s0[c] *= a.scale_log2;
+        s1[c] *= a.scale_log2;
+      }
     }
     if (pos0 + kBN - 1 > min_limit) {  // the causal diagonal crosses this tile
-      const int pm = pos0 + hsel * 32;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sm[c] = (pm + c <= limit) ? sm[c] : -INFINITY;
+      for (int c = 0; c < 32; ++c) {
+        s0[c] = (pos0 + c <= limit) ? s0[c] : -INFINITY;
+        s1[c] = (pos0 + 32 + c <= limit) ? s1[c] : -INFINITY;
+      }
     }
-    float mine;
-    {
-      float t[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) t[c] = sm[c];
-      mine = tree_max(t);
-    }
-    // the row max over both halves: exchange partial maxima with the partner warp
-    xbuf[((j & 1) * 2 + hsel) * kBM + r] = mine;
-    pair_bar(wq);
-    const float mx = fmaxf(mine, xbuf[((j & 1) * 2 + (hsel ^ 1)) * kBM + r]) * sc;
+    const float mx = fmaxf(max32(s0), max32(s1)) * sc;
     const float m_new = fmaxf(m_used, mx);
     const bool resc = m_new > m_used + 8.f;  // always true on the first tile (m_used = -inf)
     const float m_ref = resc ? m_new : m_used;
     const float corr = resc ? ex2(m_used - m_ref) : 1.f;
-    // Pairs of columns go through Blackwell's packed fp32 arithmetic (one FMA scales two scores,
-    // one add accumulates two probabilities): the exact sum feeds the LSE, the sum of the bf16
-    // values the MMA sees (a bf16 widens exactly by a 16-bit shift) normalises O.
-    uint32_t pk[16];
-    uint64_t acc_a = f32x2(0.f, 0.f), acc_b = f32x2(0.f, 0.f), racc_a = f32x2(0.f, 0.f), racc_b = f32x2(0.f, 0.f);
     const uint64_t sc2 = f32x2(sc, sc), nm2 = f32x2(-m_ref, -m_ref);
+    float tot = 0.f, rtot = 0.f;
 #pragma unroll
-    for (int c = 0; c < 16; c += 2) {
-      float x0, x1, x2, x3;
-      split_f32x2(fma_f32x2(f32x2(sm[2 * c], sm[2 * c + 1]), sc2, nm2), x0, x1);
-      split_f32x2(fma_f32x2(f32x2(sm[2 * c + 2], sm[2 * c + 3]), sc2, nm2), x2, x3);
-      const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-      acc_a = add_f32x2(acc_a, f32x2(p0, p1));
-      acc_b = add_f32x2(acc_b, f32x2(p2, p3));
-      pk[c] = pack_bf16x2(p0, p1);
-      pk[c + 1] = pack_bf16x2(p2, p3);
-      racc_a = add_f32x2(racc_a, f32x2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)));
-      racc_b = add_f32x2(racc_b, f32x2(__uint_as_float(pk[c + 1] << 16),
-                                       __uint_as_float(pk[c + 1] & 0xffff0000u)));
+    for (int hf = 0; hf < 2; ++hf) {
+      const float(&sv)[32] = hf ? s1 : s0;
+      uint32_t pk[16];
+      uint64_t acc_a = f32x2(0.f, 0.f), acc_b = f32x2(0.f, 0.f);
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        float x0, x1, x2, x3;
+        split_f32x2(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), sc2, nm2), x0, x1);
+        split_f32x2(fma_f32x2(f32x2(sv[2 * c + 2], sv[2 * c + 3]), sc2, nm2), x2, x3);
+        const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+        acc_a = add_f32x2(acc_a, f32x2(p0, p1));
+        acc_b = add_f32x2(acc_b, f32x2(p2, p3));
+        pk[c] = pack_bf16x2(p0, p1);
+        pk[c + 1] = pack_bf16x2(p2, p3);
+        rs0 = add_bf16_lo(pk[c], rs0);
+        rs1 = add_bf16_hi(pk[c], rs1);
+        rs2 = add_bf16_lo(pk[c + 1], rs2);
+        rs3 = add_bf16_hi(pk[c + 1], rs3);
+      }
+      float e0, e1;
+      split_f32x2(add_f32x2(acc_a, acc_b), e0, e1);
+      tot += e0 + e1;
+      rtot += (rs0 + rs1) + (rs2 + rs3);
+      // P (bf16 pairs) over the first 16 columns of each 32-column half of the S buffer, the
+      // layout the PV MMA reads
+      tmem_st16(taddr + st * 64 + hf * 32, pk);
     }
-    float s0, s1, s2, s3;
-    split_f32x2(add_f32x2(acc_a, acc_b), s0, s1);
-    split_f32x2(add_f32x2(racc_a, racc_b), s2, s3);
-    l = l * corr + (s0 + s1);
-    lr = lr * corr + (s2 + s3);
+    l = l * corr + tot;
+    lr = lr * corr + rtot;
     m_used = m_ref;
-    // P (bf16 pairs) over this half's own S columns, which only this warp reads
-    tmem_st16(taddr + st * 64 + hsel * 32, pk);
 
     if (j > 0 && __any_sync(0xffffffffu, resc)) {
-      // O is rescaled only after the previous tile's PV is done (its S-buffer-free phase; that
-      // barrier cannot run a phase further ahead before this warp's P of this tile is posted)
+      // O is rescaled only after the previous tile's PV is done
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
-      {
 #pragma unroll 1
-        for (int ch = 0; ch < D / 64; ++ch) {
-          float o[32];
-          const uint32_t oc = taddr + kColO + hsel * (D / 2) + ch * 32;
-          tmem_ld32(oc, o);
-          tmem_wait_ld();
+      for (int ch = 0; ch < D / 32; ++ch) {
+        float o[32];
+        const uint32_t oc = taddr + kColO + ch * 32;
+        tmem_ld32(oc, o);
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tmem_st32(oc, o);
-        }
+        for (int i = 0; i < 32; ++i) o[i] *= corr;
+        tmem_st32(oc, o);
       }
     }
     tmem_wait_st();
     if (j == w.n_tiles - 1 && w.kv_end < pos0 + kBN) {
-      // V rows past the last needed position hold stale or unused-slot data; zero them so that
-      // P = 0 times V stays 0 in the PV MMA.
+      // V rows past the last needed position: zero them so that P = 0 times V stays 0
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j >> 1) & 1));
       if (!ok) break;
       const int r0 = w.kv_end - pos0;
@@ -529,29 +540,17 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     return;
   }
   tc_fence_after();
-  // the two halves' sums
-  float* lbuf = reinterpret_cast<float*>(smem + C::kOffL);
-  lbuf[hsel * kBM + r] = l;
-  lbuf[(2 + hsel) * kBM + r] = lr;
-  pair_bar(wq);
-  const float l_tot = l + lbuf[(hsel ^ 1) * kBM + r];
-  // O is normalised by the sum of the rounded probabilities it was accumulated with, so each
-  // output row is an exact convex combination of V rows (bf16 P then adds no bias of its own)
-  const float inv = 1.f / (lr + lbuf[(2 + (hsel ^ 1)) * kBM + r]);
-  // The normalised O tile goes through shared memory so that the stores to `out` are coalesced
-  // (a thread owns one row; storing rows directly scatters every warp store over 32 rows).  The
-  // Q buffer is free: every QK has completed.  Row r's 16-byte chunk c sits at chunk
-  // c ^ (r % kChunks) of its 2D-byte line, which spreads a warp's column of chunks over the banks.
+  const float inv = 1.f / lr;
   constexpr int kCh = C::kChunks;
   uint8_t* stage = smem + C::kOffQ;
 #pragma unroll 1
-  for (int ch = 0; ch < D / 64; ++ch) {
+  for (int ch = 0; ch < D / 32; ++ch) {
     float o[32];
-    tmem_ld32(taddr + kColO + hsel * (D / 2) + ch * 32, o);
+    tmem_ld32(taddr + kColO + ch * 32, o);
     tmem_wait_ld();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int c = hsel * (kCh / 2) + ch * 4 + q;
+      const int c = ch * 4 + q;
       *reinterpret_cast<uint4*>(stage + r * (kCh * 16) + ((c ^ (r & (kCh - 1))) << 4)) =
           make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
                      pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
@@ -559,10 +558,9 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
                      pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
     }
   }
-  if (valid && hsel == 0 && a.lse)
-    a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l_tot)) * kLn2;
+  if (valid && a.lse)
+    a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l)) * kLn2;
   softmax_bar();
-  // 128 rows x kCh chunks: a warp stores whole 2D-byte rows per instruction
 #pragma unroll
   for (int k = 0; k < kBM * kCh / (kSoftmaxWarps * 32); ++k) {
     const int i = tid + k * kSoftmaxWarps * 32;
@@ -666,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0 || warp == 10) {
+  if (warp == 0 || warp == kVWarp) {
     if (kRows)
       extend_producer_rows<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
     else
@@ -679,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       if (!mbar_wait(&bars->qk_done, 0)) report(a.err_word, PKV_DEVERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == 11) {
+  } else if (warp == kPVWarp) {
     if (lane == 0) {
       if (!extend_mma_pv<D>(bars, sb, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
       umma_commit(&bars->pv_done);
