@@ -83,6 +83,7 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct ExtendArgs {
   CUtensorMap tm_q;
+  CUtensorMap tm_o;  // out viewed like q: the box of a full Q tile is stored by TMA
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   const int32_t* qo_indptr;
@@ -121,6 +122,24 @@ struct Work {
   int h, b, q0, qo0, E, t0, mask0, L, kv_end, n_tiles;
 };
 
+// The request's page list as the TMA producers read it: its offset and length, and a register
+// window of 64 entries (lane i holds entries i and 32 + i), loaded before the CTA's set-up
+// barrier so that the first K/V boxes do not wait on it.
+struct PageWindow {
+  int p0, np;
+  int32_t w0, w1;
+};
+
+__device__ __forceinline__ PageWindow load_page_window(const ExtendArgs& a, const Work& w) {
+  const int lane = threadIdx.x & 31;
+  PageWindow pw;
+  pw.p0 = __ldg(a.kv_indptr + w.b);
+  pw.np = __ldg(a.kv_indptr + w.b + 1) - pw.p0;
+  pw.w0 = lane < pw.np ? __ldg(a.kv_indices + pw.p0 + lane) : -1;
+  pw.w1 = 32 + lane < pw.np ? __ldg(a.kv_indices + pw.p0 + 32 + lane) : -1;
+  return pw;
+}
+
 // Producer warp: Q once, then K and V tiles page by page.  Lane i issues box i of a tile; the
 // page indices come from a register window of 64 page-list entries whose upper half is loaded
 // 32 pages before it is needed, so no TMA waits on a dependent global load.
@@ -128,19 +147,11 @@ struct Work {
 // ahead of the QK MMAs even while the V stream waits for its stage to be freed by PV.  The
 // warp returns only when its copies have landed (bounded waits).
 template <int D>
-__device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
+__device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv,
+                                const PageWindow& pw) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
-  const int G = a.group;
-  if (kv == 0 && lane == 0) {
-    // one box per 64-dim half: [64 dims x G heads x tokens_per_tile tokens], rows_used rows
-    mbar_arrive_expect_tx(&bars->q_full, C::kHalves * a.rows_used * 128);
-#pragma unroll
-    for (int hf = 0; hf < C::kHalves; ++hf)
-      tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * G, w.q0 + w.t0, &bars->q_full);
-  }
-  const int p0 = __ldg(a.kv_indptr + w.b);
-  const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
+  const int p0 = pw.p0, np = pw.np;
   const int R = min(a.page_size, kBN);  // rows per box (a power of two, >= 8)
   const int nbox = kBN / R;             // boxes per tile (<= 8)
   auto entry = [&](int pidx) -> int32_t {
@@ -150,7 +161,7 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
   uint64_t* empties = kv ? bars->v_empty : bars->k_empty;
   const CUtensorMap* tm = kv ? &a.tm_v : &a.tm_k;
   int wbase = 0;
-  int32_t w0 = entry(lane), w1 = entry(32 + lane);
+  int32_t w0 = pw.w0, w1 = pw.w1;
   int issued = 0;
   bool ok = true;
   for (int j = 0; j < w.n_tiles; ++j) {
@@ -221,13 +232,6 @@ template <int D>
 __device__ bool extend_producer_rows(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
-  const int G = a.group;
-  if (kv == 0 && lane == 0) {
-    mbar_arrive_expect_tx(&bars->q_full, C::kHalves * a.rows_used * 128);
-#pragma unroll
-    for (int hf = 0; hf < C::kHalves; ++hf)
-      tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * G, w.q0 + w.t0, &bars->q_full);
-  }
   const int p0 = __ldg(a.kv_indptr + w.b);
   const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
   const int ps = a.page_size;
@@ -541,7 +545,11 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
   tc_fence_after();
   const float inv = 1.f / lr;
-  constexpr int kCh = C::kChunks;
+  // The normalised O tile goes to shared memory in the layout of the Q tile's TMA boxes (64-dim
+  // halves of 128-byte rows, 16-byte chunk c of row r at chunk c ^ (r % 8)), over the Q buffer,
+  // which every QK has finished with.  A full tile then leaves by two TMA stores issued by one
+  // thread; the last, partial tile of a request (whose box would reach into the next request's
+  // rows) is copied out by the four warps with coalesced 16-byte stores.
   uint8_t* stage = smem + C::kOffQ;
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
@@ -550,8 +558,8 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     tmem_wait_ld();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int c = ch * 4 + q;
-      *reinterpret_cast<uint4*>(stage + r * (kCh * 16) + ((c ^ (r & (kCh - 1))) << 4)) =
+      const int c = ch * 4 + q;  // 16-byte chunk of the row: half c / 8, chunk c % 8 within it
+      *reinterpret_cast<uint4*>(stage + (c >> 3) * kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
           make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
                      pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
                      pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
@@ -560,17 +568,29 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
   if (valid && a.lse)
     a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l)) * kLn2;
+  fence_proxy_async_smem();  // the staged tile, before the TMA engine reads it
   softmax_bar();
+  if (w.t0 + a.tokens_per_tile <= w.E) {
+    if (tid == 0) {
 #pragma unroll
-  for (int k = 0; k < kBM * kCh / (kSoftmaxWarps * 32); ++k) {
-    const int i = tid + k * kSoftmaxWarps * 32;
-    const int row = i / kCh, c = i % kCh;
-    const int tr = a.log2_group >= 0 ? row >> a.log2_group : row / G;
-    const int t = w.t0 + tr;
-    if (row < a.rows_used && t < w.E) {
-      const int64_t orow = (int64_t)(w.qo0 + t) * a.num_q_heads + (int64_t)w.h * G + (row - tr * G);
-      reinterpret_cast<uint4*>(a.out + orow * D)[c] =
-          *reinterpret_cast<const uint4*>(stage + row * (kCh * 16) + ((c ^ (row & (kCh - 1))) << 4));
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_store_3d(&a.tm_o, hf * 64, w.h * G, w.qo0 + w.t0, smem_u32(stage + hf * kQHalf));
+      bulk_commit_group();
+      bulk_wait_group_read0();  // shared memory may be released once the stores have read it
+    }
+  } else {
+    constexpr int kCh = C::kChunks;
+#pragma unroll
+    for (int k = 0; k < kBM * kCh / (kSoftmaxWarps * 32); ++k) {
+      const int i = tid + k * kSoftmaxWarps * 32;
+      const int row = i / kCh, c = i % kCh;
+      const int tr = a.log2_group >= 0 ? row >> a.log2_group : row / G;
+      const int t = w.t0 + tr;
+      if (row < a.rows_used && t < w.E) {
+        const int64_t orow = (int64_t)(w.qo0 + t) * a.num_q_heads + (int64_t)w.h * G + (row - tr * G);
+        reinterpret_cast<uint4*>(a.out + orow * D)[c] = *reinterpret_cast<const uint4*>(
+            stage + (c >> 3) * kQHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+      }
     }
   }
 }
@@ -651,10 +671,19 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     mbar_init(&bars->p_full[0], kSoftmaxWarps);
     mbar_init(&bars->p_full[1], kSoftmaxWarps);
     fence_mbar_init();
-    prefetch_tmap(&a.tm_q);
     prefetch_tmap(&a.tm_k);
     prefetch_tmap(&a.tm_v);
+    prefetch_tmap(&a.tm_o);
+    // Q first, before the rest of the set-up: one box per 64-dim half, [64 dims x G heads x
+    // tokens_per_tile tokens], rows_used rows
+    mbar_arrive_expect_tx(&bars->q_full, C::kHalves * a.rows_used * 128);
+#pragma unroll
+    for (int hf = 0; hf < C::kHalves; ++hf)
+      tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * a.group, w.q0 + w.t0, &bars->q_full);
   }
+  // the producers' page-list window, loading while TMEM is allocated and the CTA synchronises
+  PageWindow pw{0, 0, -1, -1};
+  if (!kRows && (warp == 0 || warp == kVWarp)) pw = load_page_window(a, w);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -668,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     if (kRows)
       extend_producer_rows<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
     else
-      extend_producer<D>(a, sb, bars, w, warp == 0 ? 0 : 1);
+      extend_producer<D>(a, sb, bars, w, warp == 0 ? 0 : 1, pw);
   } else if (warp == 1) {
     if (lane == 0) {
       if (!extend_mma_qk<D>(a, sb, bars, tmem, w)) report(a.err_word, PKV_DEVERR_TIMEOUT);
@@ -820,6 +849,7 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   const uint32_t R = rows_path ? 8 : (pool->page_size < kBN ? pool->page_size : kBN);  // TMA box rows
   const uint64_t Db = (uint64_t)D * 2;
   if (!pkv_host::encode_tmap_3d(&a.tm_q, q, D, Hq, (uint64_t)num_q_rows, Db, Hq * Db, 64, G, tpt) ||
+      !pkv_host::encode_tmap_3d(&a.tm_o, out, D, Hq, (uint64_t)num_out_rows, Db, Hq * Db, 64, G, tpt) ||
       !pkv_host::encode_tmap_3d(&a.tm_k, pool->k, D, Hkv, rows, Db, Hkv * Db, 64, 1, R) ||
       !pkv_host::encode_tmap_3d(&a.tm_v, pool->v, D, Hkv, rows, Db, Hkv * Db, 64, 1, R))
     return PKV_ERR_CUDA;

@@ -19,6 +19,18 @@ PKV_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int 
       : "memory");
 }
 
+// Tiled TMA store, 3-D, shared -> global, tracked by the issuing thread's bulk async-group.
+PKV_DEV void tma_store_3d(const CUtensorMap* tm, int x, int y, int z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+PKV_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory (the
+// global writes complete on their own).
+PKV_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 PKV_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
