@@ -611,6 +611,13 @@ def run_ours(args, ws, rank, local):
                     "frac": kernels["decode"]["frac_hbm"], "traffic": traffic,
                     "algorithmic_bytes": counts["decode_bytes"],
                     "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
+    elif not ext_ms:
+        # only the append was timed: a copy, bounded by HBM bandwidth
+        k = kernels["kv_append"]
+        roofline = {"kernel": "kv_append", "bound": "hbm", "achieved": k["gbs"], "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(k["gbs"] / peaks["hbm_gbs"], 4), "traffic": None,
+                    "algorithmic_bytes": counts["append_bytes"],
+                    "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "of fallback"}
     elif counts["extend_flops"] * peaks["hbm_gbs"] >= counts["extend_bytes"] * ext_peak * 1e3:
         # arithmetic intensity at or above the ridge point: bounded by the tensor cores
         roofline = {"kernel": "paged_extend", "bound": "tensor", "achieved": kernels["extend"]["tflops"],

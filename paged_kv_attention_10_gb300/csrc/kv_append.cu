@@ -1,33 +1,54 @@
 // KV-cache write through a slot mapping, and the page gather used to check page indexing.
 //
-// Both are pure copies (bit-exact) bound by HBM bandwidth: 16-byte vector loads and stores, one
-// thread per 16-byte chunk of a token row, rows of num_kv_heads*head_dim*2 bytes.
+// Both are pure copies (bit-exact) bound by HBM bandwidth: 16-byte vector loads and stores of
+// 16-byte chunks of token rows (rows of num_kv_heads*head_dim*2 bytes).
 #include "common.cuh"
 
 namespace {
 
 using namespace pkv;
 
-// One thread per 16-byte chunk of one token's K row and the same chunk of its V row.
+// Two 16-byte chunks of token rows per thread and loop step, K and V: every load of a step (the
+// slot, two K chunks, two V chunks) is issued before any of them is used, so a thread keeps 64
+// bytes of new K/V in flight and the step costs one memory latency, not two (the slot check
+// would otherwise hold back the K/V loads).  The new rows are read once: non-caching loads.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __global__ void __launch_bounds__(256) kv_append_kernel(
     uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, const int64_t* __restrict__ slots, int32_t num_tokens,
     int32_t chunks_per_row, int64_t num_slots, uint32_t* err_word) {
   const int64_t total = (int64_t)num_tokens * chunks_per_row;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / chunks_per_row;
-    const int64_t c = i - t * chunks_per_row;
-    const int64_t slot = __ldg(slots + t);
-    if (slot < 0) continue;  // padding token
-    if (slot >= num_slots) {
-      if (c == 0) report(err_word, PKV_DEVERR_SLOT_OOB);
-      continue;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    const int64_t i1 = i0 + stride;
+    const bool has1 = i1 < total;
+    const int64_t t0 = i0 / chunks_per_row, t1 = has1 ? i1 / chunks_per_row : t0;
+    const uint4 k0 = ld_stream(k_new + i0), v0 = ld_stream(v_new + i0);
+    uint4 k1 = make_uint4(0u, 0u, 0u, 0u), v1 = k1;
+    if (has1) {
+      k1 = ld_stream(k_new + i1);
+      v1 = ld_stream(v_new + i1);
     }
-    const uint4 kv = __ldg(k_new + i);
-    const uint4 vv = __ldg(v_new + i);
-    k_pool[slot * chunks_per_row + c] = kv;
-    v_pool[slot * chunks_per_row + c] = vv;
+    const int64_t s0 = __ldg(slots + t0), s1 = __ldg(slots + t1);
+    const int64_t c0 = i0 - t0 * chunks_per_row, c1 = i1 - t1 * chunks_per_row;
+    // a negative slot is a padding token; one past the pool is reported (once per row)
+    if (s0 >= num_slots && c0 == 0) report(err_word, PKV_DEVERR_SLOT_OOB);
+    if (has1 && s1 >= num_slots && c1 == 0) report(err_word, PKV_DEVERR_SLOT_OOB);
+    if (s0 >= 0 && s0 < num_slots) {
+      k_pool[s0 * chunks_per_row + c0] = k0;
+      v_pool[s0 * chunks_per_row + c0] = v0;
+    }
+    if (has1 && s1 >= 0 && s1 < num_slots) {
+      k_pool[s1 * chunks_per_row + c1] = k1;
+      v_pool[s1 * chunks_per_row + c1] = v1;
+    }
   }
 }
 
@@ -88,8 +109,8 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
   const int32_t chunks = (int32_t)(row_bytes / 16);
   const int64_t total = (int64_t)num_tokens * chunks;
   const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = (int64_t)pkv_host::sm_count() * 16;
+  int64_t blocks = (total + 2 * threads - 1) / (2 * threads);  // two chunks per thread and step
+  const int64_t cap = (int64_t)pkv_host::sm_count() * 8;
   if (cap > 0 && blocks > cap) blocks = cap;
   kv_append_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
       (uint4*)pool->k, (uint4*)pool->v, (const uint4*)k_new, (const uint4*)v_new, slot_mapping,
