@@ -750,6 +750,10 @@ def run_reference(args, ws, rank):
         return None
     import oracle
 
+    import torch as _t
+
+    cores = args.cpu_threads if args.cpu_threads > 0 else len(os.sched_getaffinity(0))
+    _t.set_num_threads(cores)
     b = load_workload(args.workload)
     kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, b.page_size)
     run = _oracle_sample_runner(b, kp, vp)
@@ -764,7 +768,6 @@ def run_reference(args, ws, rank):
         if time.perf_counter() - t0 > budget:
             break
     el = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0))
     val = toks / el
     return {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "steps_completed": done, "warmup": args.warmup,
