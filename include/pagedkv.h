@@ -239,8 +239,8 @@ pkv_status pkv_paged_decode_noalloc(const pkv_pool* pool, const void* q, int32_t
 
 /*
  * Bytes of workspace pkv_paged_extend needs: the order in which its grid visits the requests
- * (longest KV first), int32 per request, for batches of up to 4096 requests; 0 above that (batch
- * order).
+ * (longest KV first), int32 per request, for batches of 33 to 4096 requests.  0 for up to 32
+ * requests (the kernel ranks them itself) and above 4096 (batch order).
  */
 size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_extend_len);

@@ -102,7 +102,10 @@ struct ExtendArgs {
   int32_t log2_group;  // log2(group) when the group is a power of two, else -1 (divide)
   int32_t tokens_per_tile;
   float scale_log2;
-  const int32_t* order;  // request of grid z-index z, longest KV first (nullable: batch order)
+  const int32_t* order;  // request of grid z-index z, longest KV first (nullable: ranked in the
+                         // kernel when rank_inline, else batch order)
+  int32_t rank_inline;   // batch_size <= 32: each warp ranks the requests itself
+  int32_t batch;         // requests (or parts)
   // shared-prefix parts (the unmasked instance): part b's rows q_start[b] .. + q_len[b] of q attend to all
   // prefix_lens[b] positions of its page list and write rows o_start[b] .. of out
   const int32_t* q_start;
@@ -595,6 +598,26 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   }
 }
 
+// The request that is z-th in the order "longest KV first, ties by index" (the order kernel's
+// order), computed by each warp for batches of up to 32 requests: lane i holds request i's KV
+// length and counts the requests that come before it.  Saves the order kernel's launch.
+template <bool kCausal>
+__device__ __forceinline__ int rank_request(const ExtendArgs& a, int z) {
+  const int lane = threadIdx.x & 31;
+  int64_t len = -1;  // lanes past the batch sort last
+  if (lane < a.batch) {
+    len = max(0, __ldg(a.prefix_lens + lane));
+    if (kCausal) len += max(0, __ldg(a.qo_indptr + lane + 1) - __ldg(a.qo_indptr + lane));
+  }
+  int rank = 0;
+  for (int j = 0; j < a.batch; ++j) {
+    const int64_t lj = __shfl_sync(0xffffffffu, len, j);
+    rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < a.batch && rank == z);
+  return hit ? __ffs(hit) - 1 : z;
+}
+
 template <bool kCausal, int D, bool kRows>
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
   using C = Cfg<D>;
@@ -603,7 +626,13 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   // later tiles of a request attend over more positions: launch them first
   w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
   w.h = blockIdx.y;
-  w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
+  if (a.order) {
+    w.b = __ldg(a.order + blockIdx.z);
+  } else if (a.rank_inline) {
+    w.b = rank_request<kCausal>(a, (int)blockIdx.z);
+  } else {
+    w.b = (int)blockIdx.z;
+  }
   if (kCausal) {
     w.qo0 = __ldg(a.qo_indptr + w.b);
     w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
@@ -729,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
 // the most work first and the last wave holds short ones: a bitonic sort of (length, index) keys
 // in shared memory by one CTA.  n is a power of two >= B.
 constexpr int kMaxOrdered = 4096;
+constexpr int kInlineRanked = 32;
 
 __global__ void __launch_bounds__(1024) extend_order_kernel(const int32_t* __restrict__ qo_indptr,
                                                             const int32_t* __restrict__ prefix_lens,
@@ -786,7 +816,8 @@ size_t pkv_extend_workspace_size(int32_t batch_size, int32_t num_q_heads, int32_
   (void)head_dim;
   (void)max_extend_len;
   // the request order (int32 per request) when the batch is small enough to sort in one CTA
-  if (batch_size <= 0 || batch_size > kMaxOrdered) return 0;
+  // (batches of up to kInlineRanked requests are ranked inside the extend kernel: no workspace)
+  if (batch_size <= kInlineRanked || batch_size > kMaxOrdered) return 0;
   return ((size_t)batch_size * 4 + 255) & ~(size_t)255;
 }
 
@@ -873,6 +904,8 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   a.tokens_per_tile = tpt;
   a.scale_log2 = sm_scale * kLog2e;
   a.order = nullptr;
+  a.rank_inline = batch_size <= kInlineRanked ? 1 : 0;
+  a.batch = batch_size;
   a.q_start = q_start;
   a.o_start = o_start;
   a.q_len = q_len;

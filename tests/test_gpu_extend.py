@@ -219,9 +219,13 @@ def test_extend_host_checks(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool)
     assert e.value.status == 2  # group size 17
+    # up to 32 requests are ranked inside the kernel (no workspace); more take the order kernel's
     b = random_small_batch(24, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
                            extend=[(4, 4), (0, 9)])
-    need = lib.extend_workspace_size(2, 8, 2, 128, b.max_extend_len)
+    assert lib.extend_workspace_size(2, 8, 2, 128, b.max_extend_len) == 0
+    b = random_small_batch(24, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                           extend=[(4, 4), (0, 9)] * 20)
+    need = lib.extend_workspace_size(40, 8, 2, 128, b.max_extend_len)
     assert need > 0
     with pytest.raises(lib.PagedKVError) as e:
         run_extend(lib, b, b.k_pool, b.v_pool,
