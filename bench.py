@@ -413,9 +413,11 @@ def run_ours(args, ws, rank, local):
         decode_ctas = sms - 16 if overlap and not args.eager else 0
 
     def step_branches(f=bufs):
+        # the extend branch forks once the decodes' tokens are appended, so the decode's
+        # persistent CTAs are dispatched before the extend branch's kernels can take their SMs
+        append_range(f, 0, nd_new, st)
         fork_ev.record(st)
         st2.wait_event(fork_ev)
-        append_range(f, 0, nd_new, st)
         decode(f, st)
         append_range(f, nd_new, f.kn.shape[0], st2)
         extend(f, st2)
