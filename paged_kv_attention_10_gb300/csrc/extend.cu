@@ -31,7 +31,8 @@
 //    rarely), keeps two sums of the probabilities (the exact one for the LSE; the one of the bf16
 //    values the PV MMA uses, accumulated straight from the packed bf16 pairs by the sm_100
 //    family's mixed-precision add, for O), and finally normalises its O row into a shared-memory
-//    tile that the four warps copy out with coalesced stores.
+//    tile in the Q box layout, which leaves by TMA tensor stores (a request's last, partial tile
+//    by coalesced stores of the four warps).
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include <atomic>
@@ -121,25 +122,40 @@ struct ExtendArgs {
 
 struct Work {
   // q0 / qo0: first query row of the request in q / in out; row i of the request sees the KV
-  // positions j <= min(mask0 + i, L - 1)
-  int h, b, q0, qo0, E, t0, mask0, L, kv_end, n_tiles;
+  // positions j <= min(mask0 + i, L - 1); p0 / np: its page list's offset and length
+  int h, b, q0, qo0, E, P, p0, np, t0, mask0, L, kv_end, n_tiles;
 };
+
+// A request's (or part's) metadata: its rows, KV length and page list, as one round of
+// independent loads.
+template <bool kCausal>
+__device__ __forceinline__ void load_request(const ExtendArgs& a, int b, Work& w) {
+  if (kCausal) {
+    w.qo0 = __ldg(a.qo_indptr + b);
+    w.E = __ldg(a.qo_indptr + b + 1) - w.qo0;
+    w.q0 = w.qo0;
+  } else {
+    w.q0 = __ldg(a.q_start + b);
+    w.qo0 = __ldg(a.o_start + b);
+    w.E = __ldg(a.q_len + b);
+  }
+  w.P = __ldg(a.prefix_lens + b);
+  w.p0 = __ldg(a.kv_indptr + b);
+  w.np = __ldg(a.kv_indptr + b + 1) - w.p0;
+}
 
 // The request's page list as the TMA producers read it: its offset and length, and a register
 // window of 64 entries (lane i holds entries i and 32 + i), loaded before the CTA's set-up
 // barrier so that the first K/V boxes do not wait on it.
 struct PageWindow {
-  int p0, np;
   int32_t w0, w1;
 };
 
 __device__ __forceinline__ PageWindow load_page_window(const ExtendArgs& a, const Work& w) {
   const int lane = threadIdx.x & 31;
   PageWindow pw;
-  pw.p0 = __ldg(a.kv_indptr + w.b);
-  pw.np = __ldg(a.kv_indptr + w.b + 1) - pw.p0;
-  pw.w0 = lane < pw.np ? __ldg(a.kv_indices + pw.p0 + lane) : -1;
-  pw.w1 = 32 + lane < pw.np ? __ldg(a.kv_indices + pw.p0 + 32 + lane) : -1;
+  pw.w0 = lane < w.np ? __ldg(a.kv_indices + w.p0 + lane) : -1;
+  pw.w1 = 32 + lane < w.np ? __ldg(a.kv_indices + w.p0 + 32 + lane) : -1;
   return pw;
 }
 
@@ -154,7 +170,7 @@ __device__ bool extend_producer(const ExtendArgs& a, uint32_t sb, Bars* bars, co
                                 const PageWindow& pw) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
-  const int p0 = pw.p0, np = pw.np;
+  const int p0 = w.p0, np = w.np;
   const int R = min(a.page_size, kBN);  // rows per box (a power of two, >= 8)
   const int nbox = kBN / R;             // boxes per tile (<= 8)
   auto entry = [&](int pidx) -> int32_t {
@@ -235,8 +251,7 @@ template <int D>
 __device__ bool extend_producer_rows(const ExtendArgs& a, uint32_t sb, Bars* bars, const Work& w, int kv) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
-  const int p0 = __ldg(a.kv_indptr + w.b);
-  const int np = __ldg(a.kv_indptr + w.b + 1) - p0;
+  const int p0 = w.p0, np = w.np;
   const int ps = a.page_size;
   const __nv_bfloat16* pool = kv ? a.v_pool : a.k_pool;
   uint64_t* fulls = kv ? bars->v_full : bars->k_full;
@@ -599,15 +614,18 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
 }
 
 // The request that is z-th in the order "longest KV first, ties by index" (the order kernel's
-// order), computed by each warp for batches of up to 32 requests: lane i holds request i's KV
-// length and counts the requests that come before it.  Saves the order kernel's launch.
+// order), computed by each warp for batches of up to 32 requests: lane i loads request i's
+// metadata and counts the requests that come before it, and the z-th request's metadata is then
+// taken from its lane.  Saves the order kernel's launch and a round of dependent loads.
 template <bool kCausal>
-__device__ __forceinline__ int rank_request(const ExtendArgs& a, int z) {
+__device__ __forceinline__ void rank_request(const ExtendArgs& a, int z, Work& w) {
   const int lane = threadIdx.x & 31;
+  Work mine{};
   int64_t len = -1;  // lanes past the batch sort last
   if (lane < a.batch) {
-    len = max(0, __ldg(a.prefix_lens + lane));
-    if (kCausal) len += max(0, __ldg(a.qo_indptr + lane + 1) - __ldg(a.qo_indptr + lane));
+    load_request<kCausal>(a, lane, mine);
+    len = max(0, mine.P);
+    if (kCausal) len += max(0, mine.E);
   }
   int rank = 0;
   for (int j = 0; j < a.batch; ++j) {
@@ -615,7 +633,19 @@ __device__ __forceinline__ int rank_request(const ExtendArgs& a, int z) {
     rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
   }
   const unsigned hit = __ballot_sync(0xffffffffu, lane < a.batch && rank == z);
-  return hit ? __ffs(hit) - 1 : z;
+  if (!hit) {  // not reached: the ranks of the batch are a permutation of the grid's z range
+    w.b = z;
+    load_request<kCausal>(a, z, w);
+    return;
+  }
+  const int src = __ffs(hit) - 1;
+  w.b = src;
+  w.q0 = __shfl_sync(0xffffffffu, mine.q0, src);
+  w.qo0 = __shfl_sync(0xffffffffu, mine.qo0, src);
+  w.E = __shfl_sync(0xffffffffu, mine.E, src);
+  w.P = __shfl_sync(0xffffffffu, mine.P, src);
+  w.p0 = __shfl_sync(0xffffffffu, mine.p0, src);
+  w.np = __shfl_sync(0xffffffffu, mine.np, src);
 }
 
 template <bool kCausal, int D, bool kRows>
@@ -626,21 +656,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   // later tiles of a request attend over more positions: launch them first
   w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
   w.h = blockIdx.y;
-  if (a.order) {
-    w.b = __ldg(a.order + blockIdx.z);
-  } else if (a.rank_inline) {
-    w.b = rank_request<kCausal>(a, (int)blockIdx.z);
+  if (a.rank_inline) {
+    rank_request<kCausal>(a, (int)blockIdx.z, w);
   } else {
-    w.b = (int)blockIdx.z;
-  }
-  if (kCausal) {
-    w.qo0 = __ldg(a.qo_indptr + w.b);
-    w.E = __ldg(a.qo_indptr + w.b + 1) - w.qo0;
-    w.q0 = w.qo0;
-  } else {
-    w.q0 = __ldg(a.q_start + w.b);
-    w.qo0 = __ldg(a.o_start + w.b);
-    w.E = __ldg(a.q_len + w.b);
+    w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
+    load_request<kCausal>(a, w.b, w);
   }
   // the grid covers gridDim.x * tokens_per_tile rows of each request (max_extend_len, or the
   // largest part): a request with more rows, or a negative count, is reported once, by the CTA
@@ -653,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_ROW_OOB);
     return;
   }
-  const int P = __ldg(a.prefix_lens + w.b);
+  const int P = w.P;
   if (kCausal) {
     w.mask0 = P;
     w.L = P + w.E;
@@ -711,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
       tma_load_3d(sb + C::kOffQ + hf * kQHalf, &a.tm_q, hf * 64, w.h * a.group, w.q0 + w.t0, &bars->q_full);
   }
   // the producers' page-list window, loading while TMEM is allocated and the CTA synchronises
-  PageWindow pw{0, 0, -1, -1};
+  PageWindow pw{-1, -1};
   if (!kRows && (warp == 0 || warp == kVWarp)) pw = load_page_window(a, w);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
