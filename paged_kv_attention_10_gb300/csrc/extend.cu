@@ -35,6 +35,7 @@
 //    by coalesced stores of the four warps).
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
+#include <algorithm>
 #include <atomic>
 
 #include "tc05.cuh"
@@ -106,6 +107,8 @@ struct ExtendArgs {
   const int32_t* order;  // request of grid z-index z, longest KV first (nullable: ranked in the
                          // kernel when rank_inline, else batch order)
   int32_t rank_inline;   // batch_size <= 32: each warp ranks the requests itself
+  int32_t compact;       // (causal, ranked in the kernel) grid (kv heads, Q tiles of all requests)
+  int32_t max_tiles;     // Q tiles per request the call covers: ceil(max_extend_len / tokens_per_tile)
   int32_t batch;         // requests (or parts)
   // shared-prefix parts (the unmasked instance): part b's rows q_start[b] .. + q_len[b] of q attend to all
   // prefix_lens[b] positions of its page list and write rows o_start[b] .. of out
@@ -648,29 +651,81 @@ __device__ __forceinline__ void rank_request(const ExtendArgs& a, int z, Work& w
   w.np = __shfl_sync(0xffffffffu, mine.np, src);
 }
 
+// The compact grid of a ranked batch: blockIdx.y enumerates the Q tiles of all requests, the
+// requests in the ranked order and each request's tiles last first (most KV first), with no CTA
+// for the rows a short request does not have.  Lane i loads request i's metadata and its tile
+// count T_i and sums the counts of the requests ranked before it; this CTA's request is the one
+// whose range [before, before + T) holds tile index i.  False: no tile left for this CTA.  The
+// first CTA reports a request with a negative row count or more rows than max_tiles tiles hold
+// (those rows stay unwritten, as with the full grid).
+__device__ __forceinline__ bool locate_tile(const ExtendArgs& a, int i, Work& w, bool& first_of_request) {
+  const int lane = threadIdx.x & 31;
+  Work mine{};
+  int64_t len = -1;
+  int T = 0;
+  if (lane < a.batch) {
+    load_request<true>(a, lane, mine);
+    len = (int64_t)max(0, mine.P) + max(0, mine.E);
+    T = min((max(0, mine.E) + a.tokens_per_tile - 1) / a.tokens_per_tile, a.max_tiles);
+  }
+  int before = 0, total = 0;
+  for (int j = 0; j < a.batch; ++j) {
+    const int64_t lj = __shfl_sync(0xffffffffu, len, j);
+    const int tj = __shfl_sync(0xffffffffu, T, j);
+    before += (lj > len || (lj == len && j < lane)) ? tj : 0;
+    total += tj;
+  }
+  if (i == 0 && blockIdx.x == 0) {
+    const unsigned bad = __ballot_sync(0xffffffffu, lane < a.batch &&
+                                                        (mine.E < 0 || mine.E > a.max_tiles * a.tokens_per_tile));
+    if (threadIdx.x == 0 && (bad || total > (int)gridDim.y)) report(a.err_word, PKV_DEVERR_LENGTH);
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < a.batch && i >= before && i < before + T);
+  if (!hit) return false;
+  const int src = __ffs(hit) - 1;
+  w.b = src;
+  w.q0 = __shfl_sync(0xffffffffu, mine.q0, src);
+  w.qo0 = __shfl_sync(0xffffffffu, mine.qo0, src);
+  w.E = __shfl_sync(0xffffffffu, mine.E, src);
+  w.P = __shfl_sync(0xffffffffu, mine.P, src);
+  w.p0 = __shfl_sync(0xffffffffu, mine.p0, src);
+  w.np = __shfl_sync(0xffffffffu, mine.np, src);
+  const int k = i - __shfl_sync(0xffffffffu, before, src);  // k-th tile from the request's end
+  w.t0 = (__shfl_sync(0xffffffffu, T, src) - 1 - k) * a.tokens_per_tile;
+  first_of_request = w.t0 == 0;
+  return true;
+}
+
 template <bool kCausal, int D, bool kRows>
 __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_constant__ ExtendArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Work w;
-  // later tiles of a request attend over more positions: launch them first
-  w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
-  w.h = blockIdx.y;
-  if (a.rank_inline) {
-    rank_request<kCausal>(a, (int)blockIdx.z, w);
+  bool reporter;  // the CTA that reports its request's argument errors (one per request)
+  if (kCausal && a.compact) {
+    w.h = blockIdx.x;
+    if (!locate_tile(a, (int)blockIdx.y, w, reporter)) return;
+    reporter = reporter && blockIdx.x == 0;
   } else {
-    w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
-    load_request<kCausal>(a, w.b, w);
+    // later tiles of a request attend over more positions: launch them first
+    w.t0 = (gridDim.x - 1 - blockIdx.x) * a.tokens_per_tile;
+    w.h = blockIdx.y;
+    if (a.rank_inline) {
+      rank_request<kCausal>(a, (int)blockIdx.z, w);
+    } else {
+      w.b = a.order ? __ldg(a.order + blockIdx.z) : (int)blockIdx.z;
+      load_request<kCausal>(a, w.b, w);
+    }
+    reporter = blockIdx.x == gridDim.x - 1 && blockIdx.y == 0;
+    // the grid covers gridDim.x * tokens_per_tile rows of each request (max_extend_len, or the
+    // largest part): a request with more rows, or a negative count, is reported once, by the CTA
+    // of its first tile, and its rows past the grid stay unwritten
+    if (reporter && threadIdx.x == 0 && (w.E < 0 || w.E > (int)gridDim.x * a.tokens_per_tile))
+      report(a.err_word, PKV_DEVERR_LENGTH);
+    if (w.t0 >= w.E) return;  // uniform: this tile has no rows
   }
-  // the grid covers gridDim.x * tokens_per_tile rows of each request (max_extend_len, or the
-  // largest part): a request with more rows, or a negative count, is reported once, by the CTA
-  // of its first tile, and its rows past the grid stay unwritten
-  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == 0 && threadIdx.x == 0 &&
-      (w.E < 0 || w.E > (int)gridDim.x * a.tokens_per_tile))
-    report(a.err_word, PKV_DEVERR_LENGTH);
-  if (w.t0 >= w.E) return;  // uniform: this tile has no rows
   if (w.q0 < 0 || w.qo0 < 0 || w.q0 > a.num_q_rows - w.E || w.qo0 > a.num_out_rows - w.E) {
-    if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_ROW_OOB);
+    if (threadIdx.x == 0 && reporter) report(a.err_word, PKV_DEVERR_ROW_OOB);
     return;
   }
   const int P = w.P;
@@ -683,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     w.L = max(P, 0);
     w.mask0 = w.L;
     w.kv_end = w.L;
-    if (P < 0 && threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == 0) report(a.err_word, PKV_DEVERR_LENGTH);
+    if (P < 0 && threadIdx.x == 0 && reporter) report(a.err_word, PKV_DEVERR_LENGTH);
   }
   w.n_tiles = (w.kv_end + kBN - 1) / kBN;
   if (w.n_tiles == 0) {  // a part with no KV: o = 0, lse = -inf (uniform over the CTA)
@@ -925,6 +980,13 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
   a.scale_log2 = sm_scale * kLog2e;
   a.order = nullptr;
   a.rank_inline = batch_size <= kInlineRanked ? 1 : 0;
+  const int tiles = (max_rows + tpt - 1) / tpt;
+  // the compact grid needs no more CTAs per kv head than the batch's Q tiles can number:
+  // sum_b ceil(E_b / tpt) < num_q_rows / tpt + batch
+  const int64_t compact_tiles =
+      std::min<int64_t>((int64_t)tiles * batch_size, ((int64_t)num_q_rows + tpt - 1) / tpt + batch_size);
+  a.compact = causal && a.rank_inline && compact_tiles <= 65535 ? 1 : 0;
+  a.max_tiles = tiles;
   a.batch = batch_size;
   a.q_start = q_start;
   a.o_start = o_start;
@@ -941,8 +1003,8 @@ pkv_status launch_extend(const pkv_pool* pool, const void* q, int32_t num_q_rows
     a.order = (const int32_t*)workspace;
   }
 
-  const int tiles = (max_rows + tpt - 1) / tpt;
-  dim3 grid(tiles, pool->num_kv_heads, batch_size);
+  const dim3 grid = a.compact ? dim3(pool->num_kv_heads, (unsigned)compact_tiles, 1)
+                              : dim3(tiles, pool->num_kv_heads, batch_size);
   cudaStream_t st = (cudaStream_t)stream;
   if (rows_path) {
     if (D == 128)
