@@ -677,7 +677,7 @@ __device__ __forceinline__ bool locate_tile(const ExtendArgs& a, int i, Work& w,
   }
   if (i == 0 && blockIdx.x == 0) {
     const unsigned bad = __ballot_sync(0xffffffffu, lane < a.batch &&
-                                                        (mine.E < 0 || mine.E > a.max_tiles * a.tokens_per_tile));
+                                                        (mine.E < 0 || mine.E > (int64_t)a.max_tiles * a.tokens_per_tile));
     if (threadIdx.x == 0 && (bad || total > (int)gridDim.y)) report(a.err_word, PKV_DEVERR_LENGTH);
   }
   const unsigned hit = __ballot_sync(0xffffffffu, lane < a.batch && i >= before && i < before + T);

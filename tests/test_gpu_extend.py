@@ -12,11 +12,12 @@ from _gpu_helpers import DeviceBatch, assert_attention_close, config_with_append
 pytestmark = pytest.mark.gpu
 
 
-def run_extend(lib, b, kp, vp, **kw):
+def run_extend(lib, b, kp, vp, max_extend_len=None, **kw):
     dev = "cuda"
+    mel = b.max_extend_len if max_extend_len is None else max_extend_len
     return lib.paged_extend(b.ext_q.to(dev), kp.to(dev), vp.to(dev), b.ext_qo_indptr.to(dev),
                             b.ext_kv_indptr.to(dev), b.ext_kv_indices.to(dev),
-                            b.ext_prefix_lens.to(dev), b.max_extend_len, b.sm_scale, **kw)
+                            b.ext_prefix_lens.to(dev), mel, b.sm_scale, **kw)
 
 
 def oracle_extend(b, kp, vp, **kw):
@@ -185,11 +186,14 @@ def test_extend_bad_page_index_is_reported(lib):
     assert int(err.item()) & lib.DEVERR_PAGE_OOB
 
 
-def test_extend_rows_past_max_extend_len_are_reported(lib):
+@pytest.mark.parametrize("pad", [0, 38], ids=["ranked-in-kernel", "order-kernel"])
+def test_extend_rows_past_max_extend_len_are_reported(lib, pad):
     """A max_extend_len below a request's new-token count is a caller error the kernel reports:
-    PKV_DEVERR_LENGTH, the rows the grid covers computed, the rows past it left untouched."""
+    PKV_DEVERR_LENGTH, the rows the grid covers computed, the rows past it left untouched.  Two
+    requests take the compact grid of a batch ranked in the kernel; 38 one-token requests more
+    take the full grid and the order kernel."""
     b = random_small_batch(27, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
-                           extend=[(0, 300), (50, 70)])
+                           extend=[(0, 300), (50, 70)] + [(5 + i, 1) for i in range(pad)])
     kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full_like(b.ext_q, 7.0).cuda()
@@ -231,6 +235,20 @@ def test_extend_host_checks(lib):
         run_extend(lib, b, b.k_pool, b.v_pool,
                    workspace=torch.zeros(need - 16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 3  # workspace too small for the request order
+
+
+def test_extend_huge_max_extend_len_on_a_ranked_batch(lib):
+    """A batch ranked in the kernel sizes its compact grid by the rows it has, not by
+    max_extend_len: a loose bound costs nothing and the result is unchanged."""
+    b = random_small_batch(25, page_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                           extend=[(3, 40), (90, 7)])
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_extend(lib, b, kp, vp, err_word=err, max_extend_len=2_000_000_000)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_ref, lse_ref = oracle_extend(b, kp, vp)
+    assert_attention_close(out, lse, o_ref, lse_ref, what="loose max_extend_len")
 
 
 def test_extend_speculative_verify_shape(lib):
