@@ -68,7 +68,8 @@ struct Cfg {
   static constexpr uint32_t kOffK = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffK + 2 * kKVStage;
   static constexpr uint32_t kOffBar = kOffV + 2 * kKVStage;
-  static constexpr uint32_t kSmemBytes = kOffBar + 256;
+  static constexpr uint32_t kOffInv = kOffBar + 256;  // 1 / (sum of P) of each tile row, fp32
+  static constexpr uint32_t kSmemBytes = kOffInv + kBM * 4;
   static constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of an O row
 };
 
@@ -79,7 +80,7 @@ struct Bars {
   uint64_t p_full[2];              // P of the tile in S buffer b written by the softmax
   uint64_t qk_done, pv_done;       // every MMA of the issuing thread has completed (exit path)
   uint32_t tmem_base;
-  uint32_t pad;
+  uint32_t epi_skip;  // set by a softmax thread whose waits gave up: no O to write
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -426,11 +427,6 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
   return fmaxf(max3f(b0, b1, b2), b3);
 }
 
-// barrier of all softmax warps (id 5)
-__device__ __forceinline__ void softmax_bar() {
-  asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-}
-
 // Softmax with one thread per row of the tile (four warps, one per TMEM lane quadrant): the
 // thread reads all 64 scores of its row, so the row max needs no exchange between warps.
 template <int D>
@@ -561,38 +557,57 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_free[jl & 1], (jl >> 1) & 1));
   }
   if (!ok) {
-    if (lane == 0) report(a.err_word, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) {
+      report(a.err_word, PKV_DEVERR_TIMEOUT);
+      bars->epi_skip = 1;
+    }
     return;
   }
-  tc_fence_after();
-  const float inv = 1.f / lr;
-  // The normalised O tile goes to shared memory in the layout of the Q tile's TMA boxes (64-dim
-  // halves of 128-byte rows, 16-byte chunk c of row r at chunk c ^ (r % 8)), over the Q buffer,
-  // which every QK has finished with.  A full tile then leaves by two TMA stores issued by one
-  // thread; the last, partial tile of a request (whose box would reach into the next request's
-  // rows) is copied out by the four warps with coalesced 16-byte stores.
-  uint8_t* stage = smem + C::kOffQ;
-#pragma unroll 1
-  for (int ch = 0; ch < D / 32; ++ch) {
-    float o[32];
-    tmem_ld32(taddr + kColO + ch * 32, o);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = ch * 4 + q;  // 16-byte chunk of the row: half c / 8, chunk c % 8 within it
-      *reinterpret_cast<uint4*>(stage + (c >> 3) * kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
-          make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                     pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                     pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                     pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-    }
-  }
+  // the row's normaliser for the epilogue, which all eight warps share
+  reinterpret_cast<float*>(smem + C::kOffInv)[r] = 1.f / lr;
   if (valid && a.lse)
     a.lse[(int64_t)(w.qo0 + tok) * a.num_q_heads + (int64_t)w.h * G + g] = (m_used + log2f(l)) * kLn2;
+}
+
+// Epilogue, by all eight warps once the last PV is done: the normalised O tile goes to shared
+// memory in the layout of the Q tile's TMA boxes (64-dim halves of 128-byte rows, 16-byte chunk c
+// of row r at chunk c ^ (r % 8)), over the Q buffer, which every QK has finished with.  Warp w
+// reads TMEM lane quadrant w % 4: the softmax warps read and stage the first 64 dims of their
+// rows, the producer and MMA warps (one per quadrant) the second 64, so each thread converts half
+// a row.  A full tile then leaves by two TMA stores issued by one thread; the last, partial tile
+// of a request (whose box would reach into the next request's rows) is copied out by all threads
+// with coalesced 16-byte stores.
+template <int D>
+__device__ void extend_epilogue(const ExtendArgs& a, uint8_t* smem, uint32_t tmem, const Work& w) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const bool softmax_warp = warp >= 2 && warp < 2 + kSoftmaxWarps;
+  const int G = a.group;
+  uint8_t* stage = smem + C::kOffQ;
+  tc_fence_after();
+  if (softmax_warp || C::kHalves == 2) {
+    const int hf = softmax_warp ? 0 : 1;
+    const float inv = reinterpret_cast<const float*>(smem + C::kOffInv)[r];
+    const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + kColO + hf * 64;
+    float o0[32], o1[32];
+    tmem_ld32(taddr, o0);
+    tmem_ld32(taddr + 32, o1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float(&o)[32] = q < 4 ? o0 : o1;
+      const int e = (q & 3) * 8;
+      *reinterpret_cast<uint4*>(stage + hf * kQHalf + r * 128 + ((q ^ (r & 7)) << 4)) =
+          make_uint4(pack_bf16x2(o[e] * inv, o[e + 1] * inv), pack_bf16x2(o[e + 2] * inv, o[e + 3] * inv),
+                     pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv), pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
+    }
+  }
   fence_proxy_async_smem();  // the staged tile, before the TMA engine reads it
-  softmax_bar();
+  __syncthreads();
   if (w.t0 + a.tokens_per_tile <= w.E) {
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
 #pragma unroll
       for (int hf = 0; hf < C::kHalves; ++hf)
         tma_store_3d(&a.tm_o, hf * 64, w.h * G, w.qo0 + w.t0, smem_u32(stage + hf * kQHalf));
@@ -602,8 +617,8 @@ __device__ void extend_softmax(const ExtendArgs& a, uint8_t* smem, Bars* bars, u
   } else {
     constexpr int kCh = C::kChunks;
 #pragma unroll
-    for (int k = 0; k < kBM * kCh / (kSoftmaxWarps * 32); ++k) {
-      const int i = tid + k * kSoftmaxWarps * 32;
+    for (int k = 0; k < kBM * kCh / kThreads; ++k) {
+      const int i = threadIdx.x + k * kThreads;
       const int row = i / kCh, c = i % kCh;
       const int tr = a.log2_group >= 0 ? row >> a.log2_group : row / G;
       const int t = w.t0 + tr;
@@ -774,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->p_full[0], kSoftmaxWarps);
     mbar_init(&bars->p_full[1], kSoftmaxWarps);
+    bars->epi_skip = 0;
     fence_mbar_init();
     prefetch_tmap(&a.tm_k);
     prefetch_tmap(&a.tm_v);
@@ -820,6 +836,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_extend_kernel(const __grid_
   } else {
     extend_softmax<D>(a, smem, bars, tmem, w);
   }
+  tc_fence_before();
+  __syncthreads();  // every warp is done with its stream; O is complete unless a wait gave up
+  if (!bars->epi_skip) extend_epilogue<D>(a, smem, tmem, w);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
