@@ -11,7 +11,9 @@
 //  * One CTA per (128-row Q tile, KV head, request).  The rows are (token, group head) pairs:
 //    floor(128/G) consecutive tokens times the G query heads that share the KV head (G from 1
 //    to 16), so each K/V tile loaded is used by the whole group.  Q arrives by one 3-D TMA box
-//    per 64-column half (head_dim 64 or 128).
+//    per 64-column half (head_dim 64 or 128).  A batch of up to 32 requests is ranked (longest KV
+//    first) inside the kernel and takes a compact grid, one CTA per Q tile it has, the kv heads of
+//    a tile dispatched together; larger batches take a grid sized by max_extend_len.
 //  * K and V tiles of 64 positions are gathered page by page with 3-D TMA boxes
 //    [64 dims x 1 head x min(page,64) rows] in 128-byte swizzle (other page sizes: row copies
 //    into the same layout), into 2-stage rings filled by two producer warps (K with Q, and V), so
@@ -30,9 +32,9 @@
 //    fp32 (the running max only moves when it grows by more than 2^8, so O is rescaled in TMEM
 //    rarely), keeps two sums of the probabilities (the exact one for the LSE; the one of the bf16
 //    values the PV MMA uses, accumulated straight from the packed bf16 pairs by the sm_100
-//    family's mixed-precision add, for O), and finally normalises its O row into a shared-memory
-//    tile in the Q box layout, which leaves by TMA tensor stores (a request's last, partial tile
-//    by coalesced stores of the four warps).
+//    family's mixed-precision add, for O).  At the end all eight warps normalise the O tile into
+//    shared memory in the Q box layout, half a row each, and it leaves by TMA tensor stores (a
+//    request's last, partial tile by coalesced stores of all threads).
 //  * Two CTAs fit on an SM (99 KB of shared memory and 256 TMEM columns each), so one CTA's
 //    softmax overlaps the other's MMAs.
 #include <algorithm>
