@@ -331,6 +331,10 @@ template <int D>
 __device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint32_t tmem, const Work& w) {
   using C = Cfg<D>;
   constexpr uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
+  // operand descriptors built once: a K-step or a stage only moves the start address field
+  // (address / 16 in the low 14 bits; every offset here stays inside shared memory's 256 KB)
+  const uint64_t qdesc = smem_desc_sw128(sb + C::kOffQ, 16, 1024);
+  const uint64_t kdesc0 = smem_desc_sw128(sb + C::kOffK, 16, 1024);
   if (!mbar_wait(&bars->q_full, 0)) return false;
   for (int j = 0; j < w.n_tiles; ++j) {
     const int st = j & 1;
@@ -338,12 +342,12 @@ __device__ bool extend_mma_qk(const ExtendArgs& a, uint32_t sb, Bars* bars, uint
     if (!mbar_wait(&bars->k_full[st], ph)) return false;
     if (!mbar_wait(&bars->s_free[st], ph ^ 1)) return false;
     tc_fence_after();
-    const uint32_t kb = sb + C::kOffK + st * C::kKVStage;
+    const uint64_t kdesc = kdesc0 + ((st * C::kKVStage) >> 4);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const uint64_t adesc = smem_desc_sw128(sb + C::kOffQ + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
-      const uint64_t bdesc = smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-      umma_ss(tmem + st * 64, adesc, bdesc, idesc_qk, ks > 0);
+      const uint32_t qoff = ((ks >> 2) * kQHalf + (ks & 3) * 32) >> 4;
+      const uint32_t koff = ((ks >> 2) * kKVHalf + (ks & 3) * 32) >> 4;
+      umma_ss(tmem + st * 64, qdesc + qoff, kdesc + koff, idesc_qk, ks > 0);
     }
     umma_commit(&bars->s_full[st]);
     umma_commit(&bars->k_empty[st]);
@@ -355,21 +359,21 @@ template <int D>
 __device__ bool extend_mma_pv(Bars* bars, uint32_t sb, uint32_t tmem, const Work& w) {
   using C = Cfg<D>;
   constexpr uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
+  const uint64_t vdesc0 = smem_desc_sw128(sb + C::kOffV, kKVHalf, 1024);
   for (int j = 0; j < w.n_tiles; ++j) {
     const int st = j & 1;
     const uint32_t ph = (j >> 1) & 1;
     if (!mbar_wait(&bars->p_full[st], ph)) return false;
     if (!mbar_wait(&bars->v_full[st], ph)) return false;
     tc_fence_after();
-    const uint32_t vb = sb + C::kOffV + st * C::kKVStage;
+    const uint64_t vdesc = vdesc0 + ((st * C::kKVStage) >> 4);
 #pragma unroll
     for (int ks = 0; ks < kBN / 16; ++ks) {
       // P of positions [16ks, 16ks+16): its half's columns of the tile's S buffer, bf16 pairs.
       // V rows [16ks, 16ks+16) as one MN-major operand of N = D; its 64-dim halves are kKVHalf
       // apart.
       const uint32_t pa = tmem + st * 64 + (ks >> 1) * 32 + (ks & 1) * 8;
-      const uint64_t bdesc = smem_desc_sw128(vb + ks * 2048, kKVHalf, 1024);
-      umma_ts(tmem + kColO, pa, bdesc, idesc_pv, j > 0 || ks > 0);
+      umma_ts(tmem + kColO, pa, vdesc + ((ks * 2048) >> 4), idesc_pv, j > 0 || ks > 0);
     }
     umma_commit(&bars->v_empty[st]);
     umma_commit(&bars->s_free[st]);  // P (in the S buffer) consumed; also marks this PV done
