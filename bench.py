@@ -268,6 +268,11 @@ def run_ours(args, ws, rank, local):
     inputs = [("kn", b.k_new), ("vn", b.v_new), ("sm", b.slot_mapping), ("d_ind", b.dec_kv_indptr),
               ("d_idx", b.dec_kv_indices), ("d_len", b.dec_kv_lens), ("e_qo", b.ext_qo_indptr),
               ("e_ind", b.ext_kv_indptr), ("e_idx", b.ext_kv_indices), ("e_pre", b.ext_prefix_lens)]
+    # each decode request's shared prefix length, the decode's L2 keep hint (a radix cache knows
+    # it: the length of the match other requests of the step share)
+    use_keep = not args.no_l2_keep and b.num_decode > 0
+    if use_keep:
+        inputs += [("d_keep", b.dec_shared_tokens)]
     table = None
     if args.rope:
         # the step's queries are the new tokens' (decodes first, then extend tokens, the slot
@@ -323,6 +328,7 @@ def run_ours(args, ws, rank, local):
         f.in_buf, din = _packed(inputs, dev)
         for n in ("kn", "vn", "sm", "d_ind", "d_idx", "d_len", "e_qo", "e_ind", "e_idx", "e_pre"):
             setattr(f, n, din[n])
+        f.d_keep = din["d_keep"] if use_keep else None
         if plan is not None:
             for n in ("p_qs", "p_ql", "p_os", "p_ind", "p_idx", "p_len"):
                 setattr(f, n, din[n])
@@ -358,7 +364,8 @@ def run_ours(args, ws, rank, local):
     def decode(f, stream, sub=None):
         if plan is None:
             pkv.paged_decode(f.dq, kp, vp, f.d_ind, f.d_idx, f.d_len, b.sm_scale, out=f.d_out,
-                             lse=f.d_lse, workspace=dws, stream=stream, max_ctas=decode_ctas)
+                             lse=f.d_lse, workspace=dws, stream=stream, max_ctas=decode_ctas,
+                             l2_keep_tokens=f.d_keep)
             return
         # shared pages once per group (splits 0..S-1), each request's own pages (split S), merge
         # (the scratch partial states are shared by both buffer sets: steps run in stream order)
@@ -671,6 +678,8 @@ def run_ours(args, ws, rank, local):
                             f"the shared pages ({plan.shared_tokens} tokens) on tensor cores, a decode over "
                             "each request's own pages, bf16 partial-state merge"),
             "decode_sms": decode_ctas or sms,
+            "decode_l2_keep": ("each request's shared prefix evict-last in L2, the rest evict-first"
+                               if use_keep and plan is None else "none"),
             "launch": ("eager launches" if args.eager else "CUDA graph of the whole step")
             + ("; two branches: (append of the decodes' tokens, decode, merge) beside (append of the "
                "extend tokens, extend)" if overlap else "; one stream")
@@ -849,6 +858,8 @@ def main():
     ap.add_argument("--decode-sms", type=int, default=-1,
                     help="SMs the decode may use (0 = all; default: all but 16 when the step's extend "
                          "runs beside the decode in its own graph branch, else all)")
+    ap.add_argument("--no-l2-keep", action="store_true",
+                    help="decode without the L2 keep hint for the requests' shared prefixes")
     ap.add_argument("--serial-step", action="store_true",
                     help="run the step's operations one after another on one stream (no branches)")
     ap.add_argument("--gpus", type=int, default=1,

@@ -212,6 +212,28 @@ pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t ba
                                  uint32_t* err_word, int32_t max_ctas, void* stream);
 
 /*
+ * pkv_paged_decode_ctas with an L2 residency hint for KV that several requests of the batch read:
+ * the pages of a prefix shared through the radix cache (mini-sglang README, "KVcache
+ * Management").  The decode streams every request's KV through L2 once; without a hint, a shared
+ * prefix read early in the step is evicted by the stream before the sharers that come later read
+ * it, and it is fetched from HBM again for them.
+ *   keep_tokens  nullable device int32 [batch_size]: request b's positions below keep_tokens[b]
+ *                are fetched with an evict-last L2 policy (the caller expects other requests of
+ *                the batch to read them too, e.g. its radix-cache match length when the match is
+ *                shared), every other position with evict-first.  NULL: the default policy for
+ *                every load, which is pkv_paged_decode_ctas.
+ * The hint only steers what the L2 evicts: results are bit for bit those of pkv_paged_decode_ctas
+ * with the same arguments, whatever keep_tokens holds.  Marking unshared KV evict-last makes it
+ * crowd the shared pages out instead, and marking a shared prefix 0 makes it leave first.
+ */
+pkv_status pkv_paged_decode_l2keep(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                   int32_t num_q_heads, const int32_t* kv_indptr,
+                                   const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   uint32_t* err_word, int32_t max_ctas, const int32_t* keep_tokens,
+                                   void* stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  No counterpart on the pages: this is a
  * convenience of this library.  A serving engine that reserves a fixed share of HBM for its KV
  * pool, or code that must not call cudaMalloc (and take its implicit device synchronisation) in

@@ -79,6 +79,8 @@ def load():
                                       _c_sz, _vp, _vp]),
         "pkv_paged_decode_ctas": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
                                            _vp, _c_sz, _vp, _c_i32, _vp]),
+        "pkv_paged_decode_l2keep": (_c_i32, [P, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_f32, _vp, _vp,
+                                             _vp, _c_sz, _vp, _c_i32, _vp, _vp]),
         "pkv_extend_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32]),
         "pkv_paged_extend": (_c_i32, [P, _vp, _c_i32, _vp, _c_i32, _c_i32, _vp, _vp, _vp, _c_i32,
                                       _c_f32, _vp, _vp, _vp, _c_sz, _vp, _vp]),
@@ -296,9 +298,13 @@ def decode_workspace_size(batch_size, num_q_heads, num_kv_heads, head_dim, devic
 
 
 def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: float, out=None,
-                 lse=None, workspace=None, err_word=None, stream=None, return_lse=True, max_ctas=0):
+                 lse=None, workspace=None, err_word=None, stream=None, return_lse=True, max_ctas=0,
+                 l2_keep_tokens=None):
     """Decode attention of q [B, Hq, D] over each request's paged KV. Returns (out, lse).
-    ``max_ctas`` > 0 runs it on at most that many SMs (the rest stay free for other streams)."""
+    ``max_ctas`` > 0 runs it on at most that many SMs (the rest stay free for other streams).
+    ``l2_keep_tokens`` (int32 [B] on the device): request b's first l2_keep_tokens[b] positions
+    are kept in L2 ahead of the rest (a prefix other requests of the batch share); the results
+    do not change."""
     pool = _pool(k_pool, v_pool)
     dev = k_pool.device
     _need(q, "q", torch.bfloat16, dev)
@@ -319,7 +325,15 @@ def paged_decode(q, k_pool, v_pool, kv_indptr, kv_indices, kv_lens, sm_scale: fl
         if workspace is None:
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
-        if max_ctas:
+        if l2_keep_tokens is not None:
+            _need(l2_keep_tokens, "l2_keep_tokens", torch.int32, dev)
+            if l2_keep_tokens.shape != (B,):
+                raise ValueError("l2_keep_tokens must be [batch_size]")
+            _call("pkv_paged_decode_l2keep", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
+                  _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
+                  _ptr(workspace), workspace.numel(), _ptr(err_word), int(max_ctas),
+                  _ptr(l2_keep_tokens), _stream_ptr(stream, dev))
+        elif max_ctas:
             _call("pkv_paged_decode_ctas", ctypes.byref(pool), _ptr(q), B, Hq, _ptr(kv_indptr),
                   _ptr(kv_indices), _ptr(kv_lens), float(sm_scale), _ptr(out), _ptr(lse),
                   _ptr(workspace), workspace.numel(), _ptr(err_word), int(max_ctas),

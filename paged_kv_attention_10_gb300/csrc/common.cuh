@@ -139,6 +139,12 @@ PKV_DEV uint64_t policy_evict_last() {
   return p;
 }
 
+PKV_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Warp-level fragments (m16n8k16 bf16 MMA, ldmatrix, movmatrix)
 // ---------------------------------------------------------------------------------------------

@@ -71,6 +71,7 @@ struct DecodeArgs {
   float* lse;
   float* part_o;
   float* part_lse;
+  const int32_t* keep_tokens;  // nullable: positions below keep_tokens[b] evict-last in L2, the rest evict-first
   int32_t* unit_first;
   int32_t* unit_last;
   uint32_t* err_word;
@@ -146,6 +147,9 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
     const int32_t v1 = __shfl_sync(0xffffffffu, w1, k & 31);
     return k < 32 ? v0 : v1;
   };
+
+  // L2 policies of the keep hint (made once; unused without a hint)
+  const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
 
   int nissued = 0;  // stages handed to the consumers (copies, or the end marker)
   auto next_stage = [&]() {
@@ -228,10 +232,21 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
       if (row >= 0) {
         const uint32_t slice_off = (uint32_t)lane * a.HC * 2048;
         const uint32_t half_stride = (uint32_t)W * a.HC * 2048;
+        if (a.keep_tokens) {
+          const uint64_t pol = tok < __ldg(a.keep_tokens + b) ? pol_keep : pol_stream;
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
-          tma_load_3d(smem_u32(kst) + hf * half_stride + slice_off, &a.tm_k, hf * 64, row, hg * a.HC, &full[stage]);
-          tma_load_3d(smem_u32(vst) + hf * half_stride + slice_off, &a.tm_v, hf * 64, row, hg * a.HC, &full[stage]);
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_3d_hint(smem_u32(kst) + hf * half_stride + slice_off, &a.tm_k, hf * 64, row, hg * a.HC,
+                             &full[stage], pol);
+            tma_load_3d_hint(smem_u32(vst) + hf * half_stride + slice_off, &a.tm_v, hf * 64, row, hg * a.HC,
+                             &full[stage], pol);
+          }
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_3d(smem_u32(kst) + hf * half_stride + slice_off, &a.tm_k, hf * 64, row, hg * a.HC, &full[stage]);
+            tma_load_3d(smem_u32(vst) + hf * half_stride + slice_off, &a.tm_v, hf * 64, row, hg * a.HC, &full[stage]);
+          }
         }
       }
     } else {
@@ -262,12 +277,19 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* stages, StageHdr* 
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)tot * RB * 2);
       __syncwarp();
+      const int keep = a.keep_tokens ? __ldg(a.keep_tokens + b) : 0;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         if (src[r] >= 0) {
           const int j = lane + 32 * r;
-          bulk_g2s(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage]);
-          bulk_g2s(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage]);
+          if (a.keep_tokens) {
+            const uint64_t pol = tok0 + j < keep ? pol_keep : pol_stream;
+            bulk_g2s_hint(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage], pol);
+            bulk_g2s_hint(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage], pol);
+          } else {
+            bulk_g2s(kst + (size_t)j * RS, a.k_pool + src[r], RB, &full[stage]);
+            bulk_g2s(vst + (size_t)j * RS, a.v_pool + src[r], RB, &full[stage]);
+          }
         }
       }
     }
@@ -939,6 +961,17 @@ pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t ba
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  uint32_t* err_word, int32_t max_ctas, void* stream) {
   pkv_host::NvtxRange nvtx_range("pkv_paged_decode_ctas");
+  return pkv_paged_decode_l2keep(pool, q, batch_size, num_q_heads, kv_indptr, kv_indices, kv_lens, sm_scale,
+                                 out, lse, workspace, workspace_bytes, err_word, max_ctas, nullptr, stream);
+}
+
+pkv_status pkv_paged_decode_l2keep(const pkv_pool* pool, const void* q, int32_t batch_size,
+                                   int32_t num_q_heads, const int32_t* kv_indptr,
+                                   const int32_t* kv_indices, const int32_t* kv_lens, float sm_scale,
+                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   uint32_t* err_word, int32_t max_ctas, const int32_t* keep_tokens,
+                                   void* stream) {
+  pkv_host::NvtxRange nvtx_range("pkv_paged_decode_l2keep");
   if (!pkv_host::valid_pool(pool) || batch_size < 0 || num_q_heads <= 0 || max_ctas < 0)
     return PKV_ERR_INVALID_ARG;
   if (batch_size == 0) return PKV_OK;
@@ -968,6 +1001,7 @@ pkv_status pkv_paged_decode_ctas(const pkv_pool* pool, const void* q, int32_t ba
   a.kv_indptr = kv_indptr;
   a.kv_indices = kv_indices;
   a.kv_lens = kv_lens;
+  a.keep_tokens = keep_tokens;
   a.scale_log2 = sm_scale * pkv::kLog2e;
   a.out = (__nv_bfloat16*)out;
   a.lse = lse;

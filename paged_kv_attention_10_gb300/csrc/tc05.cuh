@@ -19,6 +19,16 @@ PKV_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int 
       : "memory");
 }
 
+// The same with an L2 eviction-priority hint (a policy made by createpolicy).
+PKV_DEV void tma_load_3d_hint(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar,
+                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Tiled TMA store, 3-D, shared -> global, tracked by the issuing thread's bulk async-group.
 PKV_DEV void tma_store_3d(const CUtensorMap* tm, int x, int y, int z, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(

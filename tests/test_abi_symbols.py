@@ -34,7 +34,7 @@ def test_header_declares_the_hot_path():
               "pkv_merge_states", "pkv_decode_workspace_size", "pkv_extend_workspace_size",
               "pkv_status_string", "pkv_version", "pkv_shared_prefix_attention",
               "pkv_shared_prefix_workspace_size", "pkv_merge_states_bf16", "pkv_rope_cos_sin_table",
-              "pkv_plan_shared_prefix"):
+              "pkv_plan_shared_prefix", "pkv_paged_decode_l2keep"):
         assert n in names
 
 

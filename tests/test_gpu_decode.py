@@ -198,3 +198,29 @@ def test_decode_negative_sm_limit_rejected(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run_decode(lib, b, b.k_pool.cuda(), b.v_pool.cuda(), max_ctas=-1)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("page_size", [16, 1], ids=["tma-boxes", "row-copies"])
+def test_decode_l2_keep_hint_changes_nothing(lib, page_size):
+    """The L2 keep hint only steers the L2's evictions: with each request's shared prefix, with
+    zeros, or with values outside [0, kv_lens] the decode is bit for bit the one without a hint,
+    and within tolerance of the oracle."""
+    b = random_small_batch(41, page_size=page_size, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                           decode_lens=(40, 700, 900, 1300, 650, 90), share_decode_prefix=512)
+    kp, vp = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, page_size)
+    kpd, vpd = kp.cuda(), vp.cuda()
+    out0, lse0 = run_decode(lib, b, kpd, vpd)
+    o_ref, lse_ref = oracle.paged_decode(b.dec_q, kp, vp, b.dec_kv_indptr, b.dec_kv_indices,
+                                         b.dec_kv_lens, page_size, b.sm_scale)
+    assert_attention_close(out0, lse0, o_ref, lse_ref, what="decode without a hint")
+    out40, lse40 = run_decode(lib, b, kpd, vpd, max_ctas=40)
+    B = b.num_decode
+    hints = [b.dec_shared_tokens, torch.zeros(B, dtype=torch.int32),
+             torch.tensor([-5, 10**9, 0, 7, 2**31 - 1, -(2**31)][:B], dtype=torch.int32)]
+    for hint in hints:
+        for max_ctas, (o_plain, l_plain) in ((0, (out0, lse0)), (40, (out40, lse40))):
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            out, lse = run_decode(lib, b, kpd, vpd, l2_keep_tokens=hint.cuda(), max_ctas=max_ctas, err_word=err)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            assert torch.equal(out.view(torch.int16), o_plain.view(torch.int16)) and torch.equal(lse, l_plain)

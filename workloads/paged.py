@@ -89,6 +89,15 @@ class PagedBatch:
     shared_pages: dict = field(default_factory=dict)
 
     @property
+    def dec_shared_tokens(self) -> torch.Tensor:
+        """int32 [Bd]: how many leading positions each decode request shares with other requests
+        of the step (its share group's pages; 0 outside every group) -- what a radix cache knows
+        of each request's shared prefix."""
+        return torch.tensor([int(self.shared_pages[r.share_group].numel()) * self.page_size
+                             if r.share_group >= 0 else 0
+                             for r in self.requests if r.kind == "decode"], dtype=torch.int32)
+
+    @property
     def num_decode(self) -> int:
         return int(self.dec_kv_lens.numel())
 
