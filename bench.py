@@ -417,7 +417,7 @@ def run_ours(args, ws, rank, local):
     if args.decode_sms >= 0:
         decode_ctas = args.decode_sms
     else:
-        decode_ctas = sms - 16 if overlap and not args.eager else 0
+        decode_ctas = sms - EXTEND_SPARE_SMS if overlap and not args.eager else 0
 
     def step_branches(f=bufs):
         # the extend branch forks once the decodes' tokens are appended, so the decode's
@@ -805,6 +805,10 @@ def run_reference(args, ws, rank):
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
+
+# SMs the branched step's decode leaves to the extend beside it (swept on the mixed step: 12 of
+# 152 gave the shortest step once the decode kept its shared prefix in L2; 16 before)
+EXTEND_SPARE_SMS = 12
 
 WORKLOADS = {"mixed": 5, "tiny": 1, "batched-decode": 2, "radix-extend": 3, "long-decode": 4}
 

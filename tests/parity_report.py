@@ -58,7 +58,7 @@ def main():
             print(f"| {names[idx]} | kv_append ({b.num_new_tokens} tokens) | bit-exact: {'yes' if same else 'NO'} | | | | {'yes' if same else 'NO'} |")
             ok &= same
         if b.num_decode:
-            ctas = sms - 16 if idx == 5 else 0  # the branched step's decode leaves 16 SMs to the extend
+            ctas = sms - 12 if idx == 5 else 0  # the branched step's decode leaves 12 SMs to the extend
             out, lse = pkv.paged_decode(d.dec_q, d.k_pool, d.v_pool, d.dec_kv_indptr, d.dec_kv_indices,
                                         d.dec_kv_lens, b.sm_scale, max_ctas=ctas)
             sample = None
