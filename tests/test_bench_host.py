@@ -127,3 +127,27 @@ def test_reference_arm_json_contract():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_decode_shared_tokens_match_the_page_lists():
+    """The decode's L2 keep hint the benchmark passes: each decode request's count of leading
+    positions whose physical pages another request of the step also lists (brute force over the
+    page lists), on the mixed-step shape and a small batch."""
+    from workloads import make_config
+
+    for b in (make_config(5), random_small_batch(5, page_size=16, num_q_heads=8, num_kv_heads=2,
+                                                 head_dim=64, decode_lens=(40, 700, 900, 90),
+                                                 share_decode_prefix=32)):
+        ind, idx = b.dec_kv_indptr.tolist(), b.dec_kv_indices.tolist()
+        pages = [idx[ind[r]:ind[r + 1]] for r in range(b.num_decode)]
+        owners = {}
+        for r, pl in enumerate(pages):
+            for p in pl:
+                owners.setdefault(p, set()).add(r)
+        hint = b.dec_shared_tokens.tolist()
+        for r, pl in enumerate(pages):
+            n = 0
+            while n < len(pl) and len(owners[pl[n]]) > 1:
+                n += 1
+            assert hint[r] == n * b.page_size, (r, hint[r], n)
+        assert sum(1 for h in hint if h > 0) >= 2
