@@ -270,7 +270,7 @@ def run_ours(args, ws, rank, local):
               ("e_ind", b.ext_kv_indptr), ("e_idx", b.ext_kv_indices), ("e_pre", b.ext_prefix_lens)]
     # each decode request's shared prefix length, the decode's L2 keep hint (a radix cache knows
     # it: the length of the match other requests of the step share)
-    use_keep = not args.no_l2_keep and b.num_decode > 0
+    use_keep = not args.no_l2_keep and not args.cascade and b.num_decode > 0
     if use_keep:
         inputs += [("d_keep", b.dec_shared_tokens)]
     table = None
@@ -679,7 +679,7 @@ def run_ours(args, ws, rank, local):
                             "each request's own pages, bf16 partial-state merge"),
             "decode_sms": decode_ctas or sms,
             "decode_l2_keep": ("each request's shared prefix evict-last in L2, the rest evict-first"
-                               if use_keep and plan is None else "none"),
+                               if use_keep else "none"),
             "launch": ("eager launches" if args.eager else "CUDA graph of the whole step")
             + ("; two branches: (append of the decodes' tokens, decode, merge) beside (append of the "
                "extend tokens, extend)" if overlap else "; one stream")
