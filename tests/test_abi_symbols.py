@@ -63,6 +63,10 @@ def test_null_pool_is_rejected_before_any_cuda_call(cdll):
     f.restype = ctypes.c_int32
     assert f(None, None, ctypes.c_int32(1), ctypes.c_int32(8), None, None, None, ctypes.c_float(1.0),
              None, None, None, ctypes.c_size_t(0), None, None) == INVALID
+    f = cdll.pkv_paged_decode_l2keep
+    f.restype = ctypes.c_int32
+    assert f(None, None, ctypes.c_int32(1), ctypes.c_int32(8), None, None, None, ctypes.c_float(1.0),
+             None, None, None, ctypes.c_size_t(0), None, ctypes.c_int32(0), None, None) == INVALID
 
 
 def test_rope_table_rejects_bad_arguments_before_any_cuda_call(cdll):

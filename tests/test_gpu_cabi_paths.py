@@ -155,3 +155,39 @@ def test_rope_append_through_the_c_abi(cdll):
     keep = torch.ones(kpd.view(-1, Hkv, D).shape[0], dtype=torch.bool)
     keep[b.slot_mapping] = False
     assert bits_equal(kpd.view(-1, Hkv, D).cpu()[keep], b.k_pool.view(-1, Hkv, D)[keep])
+
+
+def test_l2keep_decode_through_the_c_abi(cdll):
+    """pkv_paged_decode_l2keep called as a C caller would: with each request's shared length it
+    returns exactly what pkv_paged_decode returns (the hint steers L2 evictions only)."""
+    ps, Hq, Hkv, D = 16, 32, 8, 128
+    b = random_small_batch(79, page_size=ps, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                           decode_lens=(40, 700, 900, 1300), decode_new=1, share_decode_prefix=256)
+    kp, vpool = oracle.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.slot_mapping, ps)
+    f = cdll.pkv_paged_decode_l2keep
+    f.argtypes = [ctypes.POINTER(Pool), vp, i32, i32, vp, vp, vp, f32, vp, vp, vp, sz, vp, i32, vp, vp]
+    f.restype = i32
+    B = b.num_decode
+    q, kpd, vpd = b.dec_q.cuda(), kp.cuda(), vpool.cuda()
+    pool = Pool(kpd.data_ptr(), vpd.data_ptr(), b.num_pages, ps, Hkv, D)
+    ind, idx, lens = b.dec_kv_indptr.cuda(), b.dec_kv_indices.cuda(), b.dec_kv_lens.cuda()
+    keep = b.dec_shared_tokens.cuda()
+    ws = cdll.pkv_decode_workspace_size(B, Hq, Hkv, D)
+    w = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for hinted in (True, False):
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        if hinted:
+            st = f(ctypes.byref(pool), _p(q), B, Hq, _p(ind), _p(idx), _p(lens), b.sm_scale, _p(out), _p(lse),
+                   _p(w), ws, _p(err), 0, _p(keep), _stream())
+        else:
+            st = cdll.pkv_paged_decode(ctypes.byref(pool), _p(q), B, Hq, _p(ind), _p(idx), _p(lens), b.sm_scale,
+                                       _p(out), _p(lse), _p(w), ws, _p(err), _stream())
+        assert st == 0
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
